@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused ZeRO-1/2 Adam step on GB300: Gelem/s and achieved HBM GB/s.
+
+One step = one call of zero_adam_step over every rank's shard (or one rank's,
+for the single-rank workload): the emulated reduce-scatter of the N ranks' bf16
+gradients, bias-corrected Adam on the fp32 master/m/v, and the bf16 cast into
+the flat parameter buffer.  Inputs are seeded and synthetic (synth/), resident
+in HBM before timing; every workload moves far more than the 129 MB L2 per
+step, so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With --gpus N > 1 (under torchrun) every rank runs an independent replica of
+the workload on its own GPU (the N emulated ZeRO ranks live inside each GPU's
+HBM; there is no cross-GPU exchange), and the value is all ranks' elements
+over the slowest rank's time.  --impl reference times the CPU oracle on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO Adam step Gelem/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _workload(name):
+    from synth import configs as C
+    if name in C.WORKLOADS:
+        return C.WORKLOADS[name]
+    if name.startswith("unit"):
+        # unit:<U>:<N>
+        _, u, n = name.split(":")
+        return C.unit_workload(int(u), int(n))
+    raise SystemExit(f"unknown workload {name}")
+
+
+def _bytes_per_step(wl, plan):
+    """Algorithmic bytes of one step: (2N + 26) per stepped element."""
+    n = _elements(wl, plan)
+    return (2 * wl.world + 26) * n
+
+
+def _elements(wl, plan):
+    if wl.rank < 0:
+        return wl.numel
+    lo = wl.rank * plan.shard
+    return max(0, min(plan.shard, wl.numel - lo))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _traffic_record(kernel_src):
+    """DRAM traffic per element from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        with open(kernel_src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        return rec.get(sha)
+    except Exception:
+        return None
+
+
+def _alloc_workload(wl, dev):
+    """Device buffers of one replica, filled by the seeded generator."""
+    import torch
+    import synth
+    import zero_partitioned_mixed_adam_gb300 as za
+    plan = za.zero_plan(wl.numel, wl.world)
+    S, P = plan.shard, plan.padded
+    single = wl.rank >= 0
+    lo = wl.rank * S if single else 0
+    n = _elements(wl, plan)
+    g_len = S if wl.grad_layout == "shard" else P
+    s_len = S if single else P
+    p_len = S if wl.param_layout == "shard" else wl.numel
+    g = [torch.zeros(g_len, dtype=torch.int16, device=dev) for _ in range(wl.world)]
+    w = torch.zeros(s_len, dtype=torch.float32, device=dev)
+    m = torch.zeros_like(w)
+    v = torch.zeros_like(w)
+    p = torch.zeros(p_len, dtype=torch.int16, device=dev)
+    st = torch.cuda.current_stream(dev).cuda_stream
+    synth.fill_dev(wl.master_spec(), lo, n, synth.OUT_F32, w.data_ptr(), st)
+    return plan, g, w, m, v, p, lo, n
+
+
+def _fill_grads(wl, g, lo, n, t, dev):
+    import torch
+    import synth
+    st = torch.cuda.current_stream(dev).cuda_stream
+    g_first = 0 if wl.grad_layout == "shard" else lo
+    for k in range(wl.world):
+        synth.fill_dev(wl.grad_spec(k, t), lo, n, synth.OUT_BF16,
+                       g[k].data_ptr() + 2 * g_first, st)
+
+
+def _step(za, wl, plan, g, w, m, v, p, t, stream):
+    za.zero_adam_step(plan, wl.rank, g, w, m, v, p, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                      eps=wl.eps, t=t,
+                      grad_layout=za.ZERO_GRAD_SHARD if wl.grad_layout == "shard" else 0,
+                      param_layout=za.ZERO_PARAM_SHARD if wl.param_layout == "shard" else 0,
+                      stream=stream)
+
+
+class OracleSample:
+    """The oracle (plain C) on a window of the workload, run over all host cores as
+    disjoint sub-windows.  Inputs are generated once; each call steps the window."""
+
+    def __init__(self, wl, max_elems=1 << 22):
+        import numpy as np
+        import synth
+        self.wl = wl
+        S = -(-wl.numel // wl.world)
+        lo = wl.rank * S if wl.rank >= 0 else 0
+        n = min(max_elems, wl.numel - lo, S if wl.rank >= 0 else wl.numel)
+        self.a, self.b, self.n = lo, lo + n, n
+        self.grads = [synth.fill_host(wl.grad_spec(k, wl.prewarm + 1), lo, n, synth.OUT_BF16)
+                      for k in range(wl.world)]
+        self.hw = synth.fill_host(wl.master_spec(), lo, n, synth.OUT_F32)
+        self.hm = np.zeros(n, np.float32)
+        self.hv = np.zeros(n, np.float32)
+        self.hp = np.zeros(n, np.uint16)
+        self.cores = os.cpu_count() or 1
+        chunk = -(-n // self.cores)
+        self.bounds = [(lo + i, min(lo + n, lo + i + chunk)) for i in range(0, n, chunk)]
+        self.t = wl.prewarm
+
+    def step(self):
+        import oracle
+        from concurrent.futures import ThreadPoolExecutor
+        wl, a = self.wl, self.a
+        self.t += 1
+        t = self.t
+
+        def run(ab):
+            oracle.zero_step(wl.numel, wl.world, -1 if wl.rank < 0 else wl.rank, self.grads,
+                             self.hw, self.hm, self.hv, self.hp, wl.lr, wl.beta1, wl.beta2,
+                             wl.eps, t, i0=ab[0], i1=ab[1], grad_base=a, state_base=a,
+                             param_base=a)
+        with ThreadPoolExecutor(max_workers=self.cores) as ex:
+            list(ex.map(run, self.bounds))
+
+    def timed(self, seconds):
+        """Step repeatedly for at least `seconds`; elements per second."""
+        done, t0 = 0, time.perf_counter()
+        while True:
+            self.step()
+            done += self.n
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return done / el, done // self.n, el
+
+    def describe(self, reps, secs):
+        return (f"window [{self.a}, {self.b}) of {self.wl.name} ({self.n} elements x "
+                f"{self.wl.world} ranks), stepped {reps} times in {secs:.1f} s on "
+                f"{self.cores} host threads (disjoint sub-windows)")
+
+
+def _cpu_oracle_sample(wl, seconds):
+    s = OracleSample(wl)
+    s.step()  # warm
+    rate, reps, secs = s.timed(seconds)
+    return {"value": rate / 1e9, "unit": "Gelem/s", "cores": s.cores, "kind": "oracle",
+            "sample": s.describe(reps, secs)}
+
+
+def run_reference(args, wl):
+    """The reference arm: the CPU oracle timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = max(0.5, min(5.0, 60.0 / max(1, args.steps + args.warmup)))
+    sample = OracleSample(wl)
+    for _ in range(args.warmup):
+        sample.step()
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        rate, reps, secs = sample.timed(per_step)
+        vals.append(rate / 1e9)
+    el = time.perf_counter() - t0
+    v = statistics.median(vals)
+    cb = {"value": v, "unit": "Gelem/s", "cores": sample.cores, "kind": "oracle",
+          "sample": sample.describe(reps, secs) + f"; median of {args.steps} such steps"}
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "Gelem/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": _config(wl, None), "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def aggregate(ms_local: float, elems_per_rank: int, world_size: int, dist=None, device=None):
+    """Whole-job throughput of N replicas: every rank's elements over the slowest rank's
+    time (max over ranks).  Returns (ms_max, Gelem/s)."""
+    ms = ms_local
+    if dist is not None and world_size > 1:
+        import torch
+        x = torch.tensor([ms_local], dtype=torch.float64,
+                         device=device if device is not None else "cpu")
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        ms = float(x.item())
+    return ms, world_size * elems_per_rank / (ms * 1e-3) / 1e9
+
+
+def _config(wl, plan):
+    c = {"workload": wl.name, "numel": wl.numel, "world": wl.world,
+         "rank": "all" if wl.rank < 0 else wl.rank, "grad_layout": wl.grad_layout,
+         "param_layout": wl.param_layout, "grad_dist": ["normal", "student_t3"][wl.grad_dist],
+         "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas",
+         "state": "fp32 master/m/v, bf16 grads and params"}
+    if plan is not None:
+        c["shard"] = plan.shard
+        c["bytes_per_step"] = _bytes_per_step(wl, plan)
+    return c
+
+
+def run_ours(args, wl):
+    import torch
+    world_size = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world_size > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import zero_partitioned_mixed_adam_gb300 as za
+
+    plan, g, w, m, v, p, lo, n = _alloc_workload(wl, dev)
+    stream = torch.cuda.current_stream(dev)
+    # prewarm steps (state as after t = 1..prewarm), then the timed gradients
+    t = 0
+    for t in range(1, wl.prewarm + 1):
+        _fill_grads(wl, g, lo, n, t, dev)
+        _step(za, wl, plan, g, w, m, v, p, t, stream)
+    _fill_grads(wl, g, lo, n, wl.prewarm + 1, dev)
+    for _ in range(args.warmup):
+        t += 1
+        _step(za, wl, plan, g, w, m, v, p, t, stream)
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        t += 1
+        ev[i][0].record(stream)
+        _step(za, wl, plan, g, w, m, v, p, t, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    elems = _elements(wl, plan)
+    bytes_step = _bytes_per_step(wl, plan)
+    ms_step, value = aggregate(total_ms / args.steps, elems, world_size, dist, dev)
+    avg_launch_ms = statistics.mean(launch_ms)
+    achieved = bytes_step / (avg_launch_ms * 1e-3) / 1e9
+    peak, peak_src = _peaks()
+    traffic = None
+    rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc",
+                                       "adam_step.cu"))
+    if rec and rec.get("world") == wl.world:
+        traffic = rec["dram_bytes_per_element"] * elems
+
+    e2e = None
+    cpu = None
+    if not args.no_e2e:
+        e2e = _e2e(args, wl, za, plan, g, w, m, v, p, lo, n, dev, stream, t, dist, world_size)
+        t += e2e.pop("_steps")
+    if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
+        cpu = _cpu_oracle_sample(wl, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": world_size,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": _config(wl, plan),
+            "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                         "kernel": "zero_adam_step_kernel",
+                         "algorithmic_bytes_per_launch": bytes_step,
+                         "avg_launch_ms": avg_launch_ms,
+                         "median_launch_ms": statistics.median(launch_ms)},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": clocks, "wall_s_timed": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def _e2e(args, wl, za, plan, g, w, m, v, p, lo, n, dev, stream, t, dist, world_size):
+    """The same step through the public API with host buffers: every step copies the
+    N ranks' gradients from pinned host memory, steps, and reads the bf16
+    parameters back, all inside the timed region."""
+    import torch
+    k_steps = max(1, min(args.steps, args.e2e_steps))
+    g_first = 0 if wl.grad_layout == "shard" else lo
+    hg = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(wl.world)]
+    for k in range(wl.world):
+        hg[k].copy_(g[k][g_first:g_first + n])
+    p_first = 0 if wl.param_layout == "shard" else lo
+    hp = torch.empty(n, dtype=torch.int16, pin_memory=True)
+    torch.cuda.synchronize(dev)
+
+    def one(tt):
+        for k in range(wl.world):
+            g[k][g_first:g_first + n].copy_(hg[k], non_blocking=True)
+        _step(za, wl, plan, g, w, m, v, p, tt, stream)
+        hp.copy_(p[p_first:p_first + n], non_blocking=True)
+
+    t += 1
+    one(t)  # warm-up
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k_steps):
+        t += 1
+        one(t)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    elems = _elements(wl, plan)
+    ms, val = aggregate(e0.elapsed_time(e1) / k_steps, elems, world_size, dist, dev)
+    return {"value": val, "unit": "Gelem/s",
+            "h2d_bytes_per_step": 2 * n * wl.world, "d2h_bytes_per_step": 2 * n,
+            "ms_per_step": ms, "steps": k_steps, "_steps": k_steps + 1}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="1p3b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--numel", type=int, default=0,
+                    help="override the workload's parameter count (smaller profiling cases)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    wl = _workload(args.workload)
+    if args.numel:
+        import dataclasses
+        wl = dataclasses.replace(wl, numel=args.numel, name=f"{wl.name}@numel={args.numel}")
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

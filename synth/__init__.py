@@ -89,6 +89,8 @@ def build_dev(force: bool = False, arch: str = "sm_103a") -> str:
         comp = arch.replace("sm_", "compute_")
         cmd = [nvcc, "-O3", f"-gencode=arch={comp},code={arch}", "-std=c++17",
                "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off", "-shared",
+               "-cudart", "shared", "-Xlinker",
+               f"-rpath,{os.path.join(os.environ.get('CUDA_HOME', '/usr/local/cuda'), 'lib64')}",
                "-o", tmp, _DEV_SRC[0]]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _DEV_SO)

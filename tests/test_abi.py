@@ -1,0 +1,166 @@
+"""The C ABI without a GPU: the library loads, exports what the header declares,
+plans layouts exactly as the oracle does, and rejects bad arguments with the
+documented status codes before touching CUDA."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def za():
+    import __graft_entry__
+    __graft_entry__.build()
+    import zero_partitioned_mixed_adam_gb300 as za
+    return za
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "zeroadam.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(zero\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declarations_are_exported(za):
+    names = _declared_functions()
+    assert set(names) == set(za.EXPORTS), names
+    lib = ctypes.CDLL(za.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_library_links_the_shared_cuda_runtime(za):
+    with open("/proc/self/maps") as f:
+        maps = f.read()
+    assert za.LIB_PATH in maps
+
+
+def test_plan_matches_oracle_brute_force(za):
+    for numel in range(1, 201):
+        for world in range(1, 18):
+            p = za.zero_plan(numel, world)
+            o = oracle.plan(numel, world)
+            for k in ("numel", "world", "shard", "pad", "padded", "bytes_dp", "bytes_z1",
+                      "bytes_z2", "bytes_z3", "state_bytes_rank"):
+                assert getattr(p, k) == o[k], (numel, world, k)
+            for k in ("formula_dp", "formula_z1", "formula_z2", "formula_z3"):
+                assert math.isclose(getattr(p, k), o[k], rel_tol=1e-15), (numel, world, k)
+
+
+def test_plan_config_sizes(za):
+    for numel, world, shard, pad in ((1_000_003, 4, 250_001, 1), (124_439_808, 8, 15_554_976, 0),
+                                     (1_300_000_000, 16, 81_250_000, 0),
+                                     (7_000_000_000, 8, 875_000_000, 0),
+                                     (202_383_360, 64, 3_162_240, 0)):
+        p = za.zero_plan(numel, world)
+        assert (p.shard, p.pad) == (shard, pad)
+
+
+def test_plan_communication_ledger(za):
+    """'The three stages' last column and 'Exercises' (second answer): DP's all-reduce
+    sends 2(N-1)/N of the bf16 gradients per card, ZeRO-1/2 exactly the same
+    (reduce-scatter + all-gather), ZeRO-3 about 1.5 times that."""
+    for world in (2, 4, 8, 16, 64):
+        numel = 10**9
+        p = za.zero_plan(numel, world)
+        grad_bytes = 2 * numel
+        assert p.comm_dp == pytest.approx(2 * (world - 1) / world * grad_bytes)
+        assert p.comm_z1 == p.comm_dp and p.comm_z2 == p.comm_dp
+        assert p.comm_z3 / p.comm_dp == pytest.approx(1.5)
+    # large N: the all-reduce sends about twice the gradient size ("about 2 x 2 Psi = 4 Psi")
+    p = za.zero_plan(10**9, 1024)
+    assert p.comm_dp / (4 * 10**9) == pytest.approx(1.0, rel=1e-3)
+
+
+def test_plan_errors(za):
+    with pytest.raises(za.ZeroError) as e:
+        za.zero_plan(0, 4)
+    assert e.value.code == "ZERO_E_NUMEL"
+    with pytest.raises(za.ZeroError) as e:
+        za.zero_plan(10, 0)
+    assert e.value.code == "ZERO_E_WORLD"
+    with pytest.raises(za.ZeroError) as e:
+        za.zero_plan(10, za.ZERO_MAX_WORLD + 1)
+    assert e.value.code == "ZERO_E_WORLD"
+    with pytest.raises(za.ZeroError) as e:
+        za.zero_plan(2**62, 1024)
+    assert e.value.code == "ZERO_E_NUMEL"
+    assert za.raw_lib().zero_plan(10, 2, None) == -1
+
+
+# Fake device addresses: every call below fails its checks before any CUDA call.
+BASE = 1 << 40
+
+
+def _step(za, plan, rank=-1, grads=None, layout=0, master=BASE + 2**30, m=BASE + 2 * 2**30,
+          v=BASE + 3 * 2**30, param=BASE + 4 * 2**30, player=0, lr=1e-3, b1=0.9, b2=0.999,
+          eps=1e-8, t=1):
+    if grads is None:
+        grads = [BASE + 5 * 2**30 + k * 2**28 for k in range(plan.world)]
+    ptrs = (ctypes.c_void_p * max(len(grads), 1))(*grads)
+    return za.raw_lib().zero_adam_step(ctypes.byref(plan), rank, ptrs, layout, master, m, v,
+                                       param, player, lr, b1, b2, eps, t, None)
+
+
+def test_step_argument_errors(za):
+    plan = za.zero_plan(1000, 4)
+    lib = za.raw_lib()
+    codes = {v: k for k, v in za.ERRORS.items()}
+    assert lib.zero_adam_step(None, -1, None, 0, 1, 1, 1, 1, 0, 1e-3, .9, .999, 1e-8, 1,
+                              None) == codes["ZERO_E_NULLPTR"]
+    assert _step(za, plan, rank=4) == codes["ZERO_E_RANK"]
+    assert _step(za, plan, rank=-2) == codes["ZERO_E_RANK"]
+    assert _step(za, plan, t=0) == codes["ZERO_E_STEP"]
+    assert _step(za, plan, lr=-1.0) == codes["ZERO_E_HPARAM"]
+    assert _step(za, plan, lr=float("nan")) == codes["ZERO_E_HPARAM"]
+    assert _step(za, plan, b1=1.0) == codes["ZERO_E_HPARAM"]
+    assert _step(za, plan, b2=-0.1) == codes["ZERO_E_HPARAM"]
+    assert _step(za, plan, eps=float("inf")) == codes["ZERO_E_HPARAM"]
+    assert _step(za, plan, layout=2) == codes["ZERO_E_LAYOUT"]
+    assert _step(za, plan, layout=1) == codes["ZERO_E_LAYOUT"]      # shard grads, all ranks
+    assert _step(za, plan, player=1) == codes["ZERO_E_LAYOUT"]      # shard params, all ranks
+    assert _step(za, plan, master=0) == codes["ZERO_E_NULLPTR"]
+    assert _step(za, plan, grads=[BASE, 0, BASE + 2**20, BASE + 2**21]) == codes["ZERO_E_NULLPTR"]
+    assert _step(za, plan, master=BASE + 2**30 + 2) == codes["ZERO_E_ALIGN"]
+    assert _step(za, plan, param=BASE + 4 * 2**30 + 1) == codes["ZERO_E_ALIGN"]
+    assert _step(za, plan, m=BASE + 2**30 + 400) == codes["ZERO_E_ALIAS"]   # m overlaps master
+    g = [BASE + 5 * 2**30 + k * 2**28 for k in range(4)]
+    assert _step(za, plan, grads=g, param=g[2] + 100) == codes["ZERO_E_ALIAS"]
+    bad = za.zero_plan(1000, 4)
+    bad.shard = 251
+    assert _step(za, bad) == codes["ZERO_E_PLAN"]
+    bad = za.zero_plan(1000, 4)
+    bad.world = 0
+    assert _step(za, bad) == codes["ZERO_E_WORLD"]
+    # single rank owning no real element: valid, nothing to do, no CUDA call
+    empty = za.zero_plan(9, 4)   # shard 3: rank 3 owns [9, 12), all padding
+    assert _step(za, empty, rank=3, layout=1, player=1) == 0
+
+
+def test_gather_argument_errors(za):
+    plan = za.zero_plan(1000, 4)
+    lib = za.raw_lib()
+    codes = {v: k for k, v in za.ERRORS.items()}
+    shards = [BASE + k * 2**20 for k in range(4)]
+    ptrs = (ctypes.c_void_p * 4)(*shards)
+    assert lib.zero3_unit_gather(ctypes.byref(plan), ptrs, None, None) == codes["ZERO_E_NULLPTR"]
+    assert lib.zero3_unit_gather(ctypes.byref(plan), None, BASE + 2**30,
+                                 None) == codes["ZERO_E_NULLPTR"]
+    assert lib.zero3_unit_gather(ctypes.byref(plan), ptrs, BASE + 2**30 + 1,
+                                 None) == codes["ZERO_E_ALIGN"]
+    assert lib.zero3_unit_gather(ctypes.byref(plan), ptrs, shards[1] - 10,
+                                 None) == codes["ZERO_E_ALIAS"]
+
+
+def test_strerror(za):
+    for code in za.ERRORS:
+        s = za.strerror(code)
+        assert s and s != "unknown status"
+    assert za.strerror(0) == "ok"
+    assert za.version() == 0x000100

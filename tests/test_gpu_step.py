@@ -1,0 +1,416 @@
+"""Parity of the fused CUDA ZeRO Adam step (through the C ABI) with the oracle.
+
+Whole vectors are compared element by element, every step, for the tiny and
+GPT-2-small workloads and for ragged sizes and misaligned buffers; the 1.3B
+and 7B workloads run at full size in the benchmark's launch configuration and
+are compared on sampled windows (rank boundaries, random windows) that the
+oracle recomputes from the same seeded inputs, plus properties that hold at
+any size.  The bar (fp32 state within 1e-6 relative, bf16 parameters within
+1 ulp) is asserted first; bit-for-bit equality is asserted after it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import configs as C
+from conftest import cuda_available
+import gpu_util as gu
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
+
+import zero_partitioned_mixed_adam_gb300 as za  # noqa: E402  (fails loudly if not built)
+
+GUARD = 512
+CANARY16 = 0x7BAD
+CANARY32 = 0x7FBADBAD  # a NaN bit pattern no computation here produces
+
+FULL, SHARD = 0, 1
+
+
+def _canary_buf(n, dtype, off):
+    """A device buffer of n elements starting `off` elements into a guarded allocation."""
+    if dtype == torch.float32:
+        base = torch.full((n + 2 * GUARD + off,), CANARY32, dtype=torch.int32, device="cuda")
+        base = base.view(torch.float32)
+    else:
+        base = torch.full((n + 2 * GUARD + off,), CANARY16, dtype=torch.int16, device="cuda")
+    return base, base[GUARD + off:GUARD + off + n]
+
+
+def _guards_intact(base, n, off):
+    b = base.view(torch.int32) if base.dtype == torch.float32 else base
+    c = CANARY32 if base.dtype == torch.float32 else CANARY16
+    head = b[:GUARD + off]
+    tail = b[GUARD + off + n:]
+    return bool((head == c).all()) and bool((tail == c).all())
+
+
+class Problem:
+    """One ZeRO step problem on the GPU, with a host mirror the oracle steps."""
+
+    def __init__(self, numel, world, rank=-1, grad_layout=FULL, param_layout=FULL, seed=0,
+                 offs=(0, 0, 0), dist=synth.NORMAL, zero_frac=0.0, lr=1e-3, b1=0.9, b2=0.999,
+                 eps=1e-8):
+        self.numel, self.world, self.rank = numel, world, rank
+        self.gl, self.pl = grad_layout, param_layout
+        self.seed, self.dist, self.zero_frac = seed, dist, zero_frac
+        self.hp = (lr, b1, b2, eps)
+        self.plan = za.zero_plan(numel, world)
+        S, P = self.plan.shard, self.plan.padded
+        self.S, self.P = S, P
+        if rank < 0:
+            self.lo, self.hi = 0, numel
+        else:
+            self.lo, self.hi = rank * S, min((rank + 1) * S, numel)
+        self.cnt = max(0, self.hi - self.lo)
+        og, os_, op = offs
+        self.offs = offs
+        g_len = P if grad_layout == FULL else S
+        s_len = P if rank < 0 else S
+        p_len = numel if param_layout == FULL else S
+        self.g_len, self.s_len, self.p_len = g_len, s_len, p_len
+        self.gbase, self.g = zip(*[_canary_buf(g_len, torch.int16, og) for _ in range(world)])
+        self.wbase, self.w = _canary_buf(s_len, torch.float32, os_)
+        self.mbase, self.m = _canary_buf(s_len, torch.float32, os_)
+        self.vbase, self.v = _canary_buf(s_len, torch.float32, os_)
+        self.pbase, self.p = _canary_buf(p_len, torch.int16, op)
+        self.p.fill_(0x1234)
+        # initial state: master from the generator at global indices, zero pad, m = v = 0
+        self.w.zero_()
+        self.m.zero_()
+        self.v.zero_()
+        s0 = 0 if rank < 0 else self.lo
+        n_real = (numel if rank < 0 else self.cnt)
+        gu.dev_fill_into(self.w[:n_real], self.master_spec(), s0, synth.OUT_F32)
+        # host mirror in the oracle's conventions: full padded gradients by global index,
+        # state by (global index - state_base), parameters as a full buffer
+        self.h_state_base = 0 if rank < 0 else self.lo
+        self.hw = np.zeros(s_len, np.float32)
+        self.hw[:n_real] = synth.fill_host(self.master_spec(), s0, n_real, synth.OUT_F32)
+        self.hm = np.zeros(s_len, np.float32)
+        self.hv = np.zeros(s_len, np.float32)
+        self.hp16 = np.full(numel, 0x1234, np.uint16)
+
+    def master_spec(self):
+        return synth.Spec(seed=self.seed, stream=C.STREAM_MASTER, sigma=0.02)
+
+    def grad_spec(self, k, t):
+        return synth.Spec(seed=self.seed, stream=C.STREAM_GRAD, rank=k, step=t, dist=self.dist,
+                          sigma=1e-3, zero_frac=self.zero_frac)
+
+    def fill_grads(self, t):
+        for k in range(self.world):
+            g = self.g[k]
+            g.zero_()
+            if self.gl == FULL:
+                gu.dev_fill_into(g[:self.numel], self.grad_spec(k, t), 0, synth.OUT_BF16)
+            else:
+                gu.dev_fill_into(g[:self.cnt], self.grad_spec(k, t), self.lo, synth.OUT_BF16)
+
+    def host_grads(self, t):
+        out = []
+        for k in range(self.world):
+            h = np.zeros(self.P, np.uint16)
+            h[:self.numel] = synth.fill_host(self.grad_spec(k, t), 0, self.numel, synth.OUT_BF16)
+            out.append(h)
+        return out
+
+    def step(self, t, stream=None):
+        lr, b1, b2, eps = self.hp
+        self.fill_grads(t)
+        za.zero_adam_step(self.plan, self.rank, list(self.g), self.w, self.m, self.v, self.p,
+                          lr=lr, beta1=b1, beta2=b2, eps=eps, t=t, grad_layout=self.gl,
+                          param_layout=self.pl, stream=stream)
+        gu.oracle_step_parallel(self.numel, self.world, self.rank, self.host_grads(t), self.hw,
+                                self.hm, self.hv, self.hp16, lr, b1, b2, eps, t,
+                                state_base=self.h_state_base)
+
+    def check(self, what=""):
+        torch.cuda.synchronize()
+        s0 = 0 if self.rank < 0 else self.lo
+        n = self.cnt if self.rank >= 0 else self.numel
+        sl = slice(0, n)
+        for name, d, h in (("master", self.w, self.hw), ("m", self.m, self.hm),
+                           ("v", self.v, self.hv)):
+            gu.assert_f32_close(gu.to_host_f32(d)[sl], h[sl], f"{what} {name}")
+            # the zero padding's state is never touched
+            assert (gu.to_host_f32(d)[n:] == 0).all(), f"{what} {name}: padding state changed"
+        dp = gu.to_host_u16(self.p)
+        p0 = self.lo if self.pl == FULL else 0
+        gu.assert_bf16_close(dp[p0:p0 + n], self.hp16[s0:s0 + n], f"{what} param")
+        outside = np.ones(dp.size, bool)
+        outside[p0:p0 + n] = False
+        assert (dp[outside] == 0x1234).all(), f"{what}: parameters outside the range written"
+        og, os_, op = self.offs
+        for k in range(self.world):
+            assert _guards_intact(self.gbase[k], self.g_len, og), f"{what}: grad {k} guard"
+        for b in (self.wbase, self.mbase, self.vbase):
+            assert _guards_intact(b, self.s_len, os_), f"{what}: state guard"
+        assert _guards_intact(self.pbase, self.p_len, op), f"{what}: param guard"
+
+
+# ------------------------------------------------------------------ tiny config
+
+
+def test_tiny_all_ranks_three_steps():
+    wl = C.TINY
+    pr = Problem(wl.numel, wl.world, seed=wl.seed)
+    assert pr.plan.shard == 250_001 and pr.plan.pad == 1
+    for t in range(1, wl.steps + 1):
+        pr.step(t)
+        pr.check(f"tiny t={t}")
+
+
+@pytest.mark.parametrize("rank", [0, 1, 2, 3])
+@pytest.mark.parametrize("layouts", [(FULL, FULL), (SHARD, FULL), (SHARD, SHARD), (FULL, SHARD)])
+def test_tiny_single_rank(rank, layouts):
+    """Rank r alone; r*shard = 250,001*r is odd for r = 1, 3 (unaligned shard starts)."""
+    wl = C.TINY
+    pr = Problem(wl.numel, wl.world, rank=rank, grad_layout=layouts[0], param_layout=layouts[1])
+    for t in (1, 2):
+        pr.step(t)
+        pr.check(f"tiny rank {rank} layouts {layouts} t={t}")
+
+
+# ---------------------------------------------------- ragged sizes, any world
+
+
+@pytest.mark.parametrize("numel,world", [
+    (1, 1), (7, 1), (8, 2), (9, 4), (15, 3), (17, 16), (100, 64), (1000, 5), (4099, 8),
+    (65537, 17), (262147, 32), (300001, 64), (20011, 65), (50000, 100), (1 << 20, 2),
+])
+def test_ragged_sizes_all_ranks(numel, world):
+    pr = Problem(numel, world, seed=numel % 7)
+    for t in (1, 2):
+        pr.step(t)
+        pr.check(f"{numel}/{world} t={t}")
+
+
+@pytest.mark.parametrize("offs", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 5), (7, 3, 7), (4, 2, 4),
+                                  (1, 1, 1)])
+def test_misaligned_buffers(offs):
+    """Buffers that start off the 16-byte grid (views into larger allocations)."""
+    pr = Problem(100_003, 4, offs=offs, seed=3)
+    for t in (1, 2):
+        pr.step(t)
+        pr.check(f"offs {offs} t={t}")
+
+
+@pytest.mark.parametrize("offs", [(1, 0, 0), (0, 1, 3), (2, 2, 2)])
+def test_misaligned_single_rank(offs):
+    pr = Problem(100_003, 4, rank=2, grad_layout=SHARD, param_layout=FULL, offs=offs)
+    pr.step(1)
+    pr.check(f"rank 2 offs {offs}")
+
+
+def test_non_default_stream():
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pr = Problem(70_001, 8)
+        pr.step(1, stream=s)
+        s.synchronize()
+    pr.check("side stream")
+
+
+def test_hyperparameter_edges():
+    """beta1 = beta2 = 0 (m = g, v = g^2), eps = 0, lr = 0 and a large step count."""
+    for hp, t in (((1e-3, 0.0, 0.0, 1e-8), 1), ((1e-3, 0.9, 0.999, 0.0), 1),
+                  ((0.0, 0.9, 0.999, 1e-8), 1), ((1e-2, 0.5, 0.75, 1e-3), 10**6)):
+        lr, b1, b2, eps = hp
+        pr = Problem(10_007, 3, lr=lr, b1=b1, b2=b2, eps=eps)
+        pr.step(t)
+        pr.check(f"hp {hp} t={t}")
+
+
+def test_special_gradient_values():
+    """Inf, NaN, denormal and huge gradients propagate exactly as in the oracle."""
+    numel, world = 4096, 4
+    pr = Problem(numel, world)
+    specials = np.array([0x7F80, 0xFF80, 0x7FC0, 0x0001, 0x8001, 0x7F7F, 0xFF7F, 0x0000, 0x8000,
+                         0x0080, 0x3F80], np.uint16)
+    rng = np.random.default_rng(11)
+    host = []
+    for k in range(world):
+        h = np.zeros(pr.P, np.uint16)
+        h[:numel] = rng.choice(specials, numel)
+        host.append(h)
+        pr.g[k].copy_(torch.from_numpy(h.view(np.int16)).cuda())
+    lr, b1, b2, eps = pr.hp
+    za.zero_adam_step(pr.plan, -1, list(pr.g), pr.w, pr.m, pr.v, pr.p, lr=lr, beta1=b1,
+                      beta2=b2, eps=eps, t=1)
+    oracle.zero_step(numel, world, -1, host, pr.hw, pr.hm, pr.hv, pr.hp16, lr, b1, b2, eps, 1)
+    pr.check("special values")
+
+
+def test_deterministic():
+    outs = []
+    for _ in range(2):
+        pr = Problem(333_333, 16, seed=9)
+        pr.fill_grads(1)
+        lr, b1, b2, eps = pr.hp
+        za.zero_adam_step(pr.plan, -1, list(pr.g), pr.w, pr.m, pr.v, pr.p, lr=lr, beta1=b1,
+                          beta2=b2, eps=eps, t=1)
+        torch.cuda.synchronize()
+        outs.append((gu.to_host_f32(pr.w).copy(), gu.to_host_u16(pr.p).copy()))
+    assert (outs[0][0].view(np.uint32) == outs[1][0].view(np.uint32)).all()
+    assert (outs[0][1] == outs[1][1]).all()
+
+
+# ---------------------------------------------------------------- GPT-2 small
+
+
+def test_gpt2_small_ten_steps_every_element():
+    """124,439,808 parameters, N = 8, 10 % shared exact-zero gradients, 10 steps, all
+    elements compared after every step.  Gradients are made on the device by the
+    generator and copied to the host for the oracle (spot-checked against the host
+    generator)."""
+    wl = C.GPT2
+    numel, world = wl.numel, wl.world
+    plan = za.zero_plan(numel, world)
+    P = plan.padded
+    g = [torch.zeros(P, dtype=torch.int16, device="cuda") for _ in range(world)]
+    w = torch.zeros(P, dtype=torch.float32, device="cuda")
+    m = torch.zeros_like(w)
+    v = torch.zeros_like(w)
+    p = torch.zeros(numel, dtype=torch.int16, device="cuda")
+    gu.dev_fill_into(w[:numel], wl.master_spec(), 0, synth.OUT_F32)
+    hw = gu.to_host_f32(w).copy()
+    gu.spot_check_generated(hw[:numel], wl.master_spec(), 0, synth.OUT_F32)
+    hm = np.zeros(P, np.float32)
+    hv = np.zeros(P, np.float32)
+    hp = np.zeros(numel, np.uint16)
+    for t in range(1, wl.steps + 1):
+        for k in range(world):
+            gu.dev_fill_into(g[k][:numel], wl.grad_spec(k, t), 0, synth.OUT_BF16)
+        za.zero_adam_step(plan, -1, g, w, m, v, p, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                          eps=wl.eps, t=t)
+        hg = [gu.to_host_u16(x) for x in g]
+        for k in range(world):
+            gu.spot_check_generated(hg[k][:numel], wl.grad_spec(k, t), 0, synth.OUT_BF16,
+                                    samples=512, seed=t * 100 + k)
+        if t == 1:
+            zero = (hg[0][:numel] == 0)
+            assert abs(zero.mean() - 0.1) < 0.01 and (hg[5][:numel][zero] == 0).all()
+        gu.oracle_step_parallel(numel, world, -1, hg, hw, hm, hv, hp, wl.lr, wl.beta1, wl.beta2,
+                                wl.eps, t)
+        gu.assert_f32_close(gu.to_host_f32(w)[:numel], hw[:numel], f"gpt2 master t={t}")
+        gu.assert_f32_close(gu.to_host_f32(m)[:numel], hm[:numel], f"gpt2 m t={t}")
+        gu.assert_f32_close(gu.to_host_f32(v)[:numel], hv[:numel], f"gpt2 v t={t}")
+        gu.assert_bf16_close(gu.to_host_u16(p), hp, f"gpt2 param t={t}")
+    del g, w, m, v, p
+    torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------- full-size, sampled windows
+
+
+def _windows(lo, hi, shard, n_random, width, rng, boundaries):
+    """Windows [a, b) inside [lo, hi): every shard boundary +-16, the first and last
+    `width` elements of each shard, and n_random random windows."""
+    ws = []
+    for b in boundaries:
+        ws.append((max(lo, b - 16), min(hi, b + 16)))
+    r0 = lo
+    while r0 < hi:
+        r1 = min(hi, r0 + shard)
+        ws.append((r0, min(r1, r0 + width)))
+        ws.append((max(r0, r1 - width), r1))
+        r0 = r1
+    for _ in range(n_random):
+        a = int(rng.integers(lo, max(lo + 1, hi - width)))
+        ws.append((a, min(hi, a + width)))
+    ws = sorted(set((a, b) for a, b in ws if b > a))
+    return ws
+
+
+def _check_windows(wl, windows, steps, dev_state, dev_param, rank, state_first):
+    """Oracle on each window for steps 1..steps from the same seeded inputs; compare
+    with the device state (index = global - state_first) and parameters (global)."""
+    for a, b in windows:
+        n = b - a
+        hw = synth.fill_host(wl.master_spec(), a, n, synth.OUT_F32)
+        hm = np.zeros(n, np.float32)
+        hv = np.zeros(n, np.float32)
+        hp = np.zeros(n, np.uint16)
+        for t in range(1, steps + 1):
+            hg = [synth.fill_host(wl.grad_spec(k, t), a, n, synth.OUT_BF16)
+                  for k in range(wl.world)]
+            oracle.zero_step(wl.numel, wl.world, rank, hg, hw, hm, hv, hp, wl.lr, wl.beta1,
+                             wl.beta2, wl.eps, t, i0=a, i1=b, grad_base=a, state_base=a,
+                             param_base=a)
+        s = slice(a - state_first, b - state_first)
+        gu.assert_f32_close(gu.to_host_f32(dev_state[0][s]), hw, f"{wl.name} master [{a},{b})")
+        gu.assert_f32_close(gu.to_host_f32(dev_state[1][s]), hm, f"{wl.name} m [{a},{b})")
+        gu.assert_f32_close(gu.to_host_f32(dev_state[2][s]), hv, f"{wl.name} v [{a},{b})")
+        gu.assert_bf16_close(gu.to_host_u16(dev_param[a:b]), hp, f"{wl.name} param [{a},{b})")
+
+
+def _param_is_cast_of_master(master, param, chunk=1 << 28):
+    """At any size: every written bf16 parameter is torch's RNE cast of the new master."""
+    for i in range(0, master.numel(), chunk):
+        ref = master[i:i + chunk].to(torch.bfloat16).view(torch.int16)
+        assert torch.equal(ref, param[i:i + chunk]), f"param != bf16(master) in chunk at {i}"
+
+
+def test_1p3b_all_ranks_full_size_sampled():
+    """Psi = 1.3e9, N = 16, Student-t(3) gradients with outliers; steps t = 1..5 are the
+    prewarm, t = 6 the first timed step; the bench's launch (all ranks, one call)."""
+    wl = C.B1P3
+    steps = wl.prewarm + wl.steps
+    plan = za.zero_plan(wl.numel, wl.world)
+    P = plan.padded
+    g = [torch.empty(P, dtype=torch.int16, device="cuda") for _ in range(wl.world)]
+    w = torch.zeros(P, dtype=torch.float32, device="cuda")
+    m = torch.zeros_like(w)
+    v = torch.zeros_like(w)
+    p = torch.zeros(wl.numel, dtype=torch.int16, device="cuda")
+    gu.dev_fill_into(w[:wl.numel], wl.master_spec(), 0, synth.OUT_F32)
+    for t in range(1, steps + 1):
+        for k in range(wl.world):
+            gu.dev_fill_into(g[k][:wl.numel], wl.grad_spec(k, t), 0, synth.OUT_BF16)
+        za.zero_adam_step(plan, -1, g, w, m, v, p, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                          eps=wl.eps, t=t)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(13)
+    bounds = [r * plan.shard for r in range(1, wl.world)]
+    wins = _windows(0, wl.numel, plan.shard, 6, 2048, rng, bounds)
+    # outliers must be present in the inputs the windows see at least once overall
+    _check_windows(wl, wins, steps, (w, m, v), p, -1, 0)
+    _param_is_cast_of_master(w[:wl.numel], p)
+    assert torch.isfinite(w).all()
+    del g, w, m, v, p
+    torch.cuda.empty_cache()
+
+
+def test_7b_rank3_full_size_sampled():
+    """Psi = 7e9, N = 8, rank 3 alone from 8 gradient slices of its 875M-element shard,
+    writing into the full 7e9-element bf16 parameter buffer; two steps."""
+    wl = C.B7_RANK3
+    plan = za.zero_plan(wl.numel, wl.world)
+    S, r = plan.shard, wl.rank
+    lo, hi = r * S, (r + 1) * S
+    g = [torch.empty(S, dtype=torch.int16, device="cuda") for _ in range(wl.world)]
+    w = torch.empty(S, dtype=torch.float32, device="cuda")
+    m = torch.zeros_like(w)
+    v = torch.zeros_like(w)
+    p = torch.full((wl.numel,), 0x1234, dtype=torch.int16, device="cuda")
+    gu.dev_fill_into(w, wl.master_spec(), lo, synth.OUT_F32)
+    steps = 2
+    for t in range(1, steps + 1):
+        for k in range(wl.world):
+            gu.dev_fill_into(g[k], wl.grad_spec(k, t), lo, synth.OUT_BF16)
+        za.zero_adam_step(plan, r, g, w, m, v, p, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                          eps=wl.eps, t=t, grad_layout=za.ZERO_GRAD_SHARD,
+                          param_layout=za.ZERO_PARAM_FULL)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(17)
+    wins = _windows(lo, hi, S, 6, 2048, rng, [lo, hi])
+    _check_windows(wl, wins, steps, (w, m, v), p, r, lo)
+    # only rank 3's range of the full parameter buffer is written
+    assert bool((p[:lo] == 0x1234).all()) and bool((p[hi:] == 0x1234).all())
+    _param_is_cast_of_master(w, p[lo:hi])
+    del g, w, m, v, p
+    torch.cuda.empty_cache()

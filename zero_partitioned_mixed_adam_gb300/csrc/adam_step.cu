@@ -1,0 +1,285 @@
+// adam_step.cu -- the fused ZeRO-1/2 optimizer step on sm_103a.
+//
+// One pass over the stepped flat range does all of "ZeRO and FSDP" ->
+// "Implementing ZeRO's Adam from scratch", ZeroAdam.step:
+//   reduce-scatter + average  : sum of the N ranks' bf16 gradients, fp32, in
+//                               rank order 0..N-1, divided by N
+//   Adam + bias correction    : fp32 master, m, v updated in place
+//   all-gather + unflatten    : bf16 (round to nearest even) of the new master
+//                               stored straight into the flat parameter buffer
+// The reduced gradient never leaves registers.  Per element the kernel moves
+// 2N (gradients) + 12 (state read) + 12 (state write) + 2 (bf16 parameter)
+// bytes and does ~20 fp32 operations: it is bound by HBM bandwidth, so it is
+// written as a streaming kernel (16-byte vector loads/stores, a persistent
+// grid-stride loop sized to the SM count) and uses no tensor cores.
+//
+// Bit-exactness: every operation is an explicit round-to-nearest intrinsic
+// (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nvcc cannot contract any
+// pair into an FMA; the library is built without fast-math, so denormals are
+// kept and division and square root are IEEE-correct.  The one rewrite is
+// g/N -> g*(1/N) when N is a power of two, which is the same correctly
+// rounded real number (1/N is exact).
+#include <cuda_bf16.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "internal.h"
+
+namespace zeroadam {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTableRuntime = 1024;  // gradient-pointer table of the any-N kernel
+
+template <int CAP>
+struct StepArgs {
+  const uint16_t* g[CAP];  // rank k's gradient, at the range's first element
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* param;
+  int64_t n;     // elements in the range
+  int64_t nvec;  // 8-element vectors in the body [head, head + 8*nvec)
+  int32_t head;  // scalar elements before the body
+  int32_t world;
+  int32_t gvec, svec, pvec;  // gradients / state / parameters 16-byte aligned in the body
+  AdamScalars s;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  return static_cast<uint32_t>(f32_to_bf16_rn(lo)) |
+         (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+}
+
+// Adam with bias correction on one element, in ZeroAdam.step's order.
+__device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, float& w, float& m,
+                                             float& v) {
+  const float g = s.pow2_world ? __fmul_rn(gsum, s.inv_world) : __fdiv_rn(gsum, s.world);
+  m = __fadd_rn(__fmul_rn(m, s.b1), __fmul_rn(s.omb1, g));
+  v = __fadd_rn(__fmul_rn(v, s.b2), __fmul_rn(__fmul_rn(s.omb2, g), g));
+  const float m_hat = __fdiv_rn(m, s.bc1);
+  const float v_hat = __fdiv_rn(v, s.bc2);
+  const float denom = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
+  w = __fsub_rn(w, __fdiv_rn(__fmul_rn(s.lr, m_hat), denom));
+}
+
+// acc[j] += rank-k gradient of element e0+j, for a 16-byte vector of 8 bf16.
+__device__ __forceinline__ void accumulate8(float acc[8], const uint4 r) {
+  acc[0] = __fadd_rn(acc[0], bf16_lo(r.x));
+  acc[1] = __fadd_rn(acc[1], bf16_hi(r.x));
+  acc[2] = __fadd_rn(acc[2], bf16_lo(r.y));
+  acc[3] = __fadd_rn(acc[3], bf16_hi(r.y));
+  acc[4] = __fadd_rn(acc[4], bf16_lo(r.z));
+  acc[5] = __fadd_rn(acc[5], bf16_hi(r.z));
+  acc[6] = __fadd_rn(acc[6], bf16_lo(r.w));
+  acc[7] = __fadd_rn(acc[7], bf16_hi(r.w));
+}
+
+// Sum over ranks of 8 consecutive elements.  The accumulator starts at -0.0,
+// the exact identity of IEEE addition (-0 + x == x for every x, +0 included),
+// so the result equals g_0 + g_1 + ... + g_{N-1} evaluated from g_0.
+template <int NT, int CAP>
+__device__ __forceinline__ void sum_grads8(const StepArgs<CAP>& a, int world, int64_t e0,
+                                           float acc[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = -0.0f;
+  if (a.gvec) {
+    // Ranks in groups: all of a group's 16-byte loads are issued before any
+    // of them is consumed, so up to G*16 bytes per thread are in flight.
+    constexpr int G = (NT > 0 && NT <= 16) ? NT : 8;
+#pragma unroll 1
+    for (int k0 = 0; k0 < world; k0 += G) {
+      uint4 r[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j)
+        if (NT > 0 || k0 + j < world)
+          r[j] = __ldcs(reinterpret_cast<const uint4*>(a.g[k0 + j] + e0));
+#pragma unroll
+      for (int j = 0; j < G; ++j)
+        if (NT > 0 || k0 + j < world) accumulate8(acc, r[j]);
+    }
+  } else {
+#pragma unroll 1
+    for (int k = 0; k < world; ++k) {
+      uint16_t h[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[j] = __ldcs(a.g[k] + e0 + j);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], bf16_to_f32(h[j]));
+    }
+  }
+}
+
+__device__ __forceinline__ void load_f32x8(const float* p, bool vec, float x[8]) {
+  if (vec) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __ldcs(p + j);
+  }
+}
+
+__device__ __forceinline__ void store_f32x8(float* p, bool vec, const float x[8]) {
+  if (vec) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+    __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(x[4], x[5], x[6], x[7]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) __stcs(p + j, x[j]);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x8_rn(uint16_t* p, bool vec, const float x[8]) {
+  if (vec) {
+    const uint4 r = make_uint4(pack_bf16x2_rn(x[0], x[1]), pack_bf16x2_rn(x[2], x[3]),
+                               pack_bf16x2_rn(x[4], x[5]), pack_bf16x2_rn(x[6], x[7]));
+    __stcs(reinterpret_cast<uint4*>(p), r);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) __stcs(reinterpret_cast<unsigned short*>(p) + j, f32_to_bf16_rn(x[j]));
+  }
+}
+
+// One element, no vector access (range head and tail).
+template <int NT, int CAP>
+__device__ __forceinline__ void step_element(const StepArgs<CAP>& a, int world, int64_t e) {
+  float acc = -0.0f;
+#pragma unroll 1
+  for (int k = 0; k < world; ++k) acc = __fadd_rn(acc, bf16_to_f32(__ldcs(a.g[k] + e)));
+  float w = a.master[e], mm = a.m[e], vv = a.v[e];
+  adam_element(acc, a.s, w, mm, vv);
+  a.master[e] = w;
+  a.m[e] = mm;
+  a.v[e] = vv;
+  a.param[e] = f32_to_bf16_rn(w);
+}
+
+template <int NT, int CAP>
+__global__ void __launch_bounds__(kThreads)
+    zero_adam_step_kernel(const __grid_constant__ StepArgs<CAP> a) {
+  const int world = NT > 0 ? NT : a.world;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+
+  for (int64_t q = tid; q < a.nvec; q += nthreads) {
+    const int64_t e0 = a.head + 8 * q;
+    float acc[8], w[8], mm[8], vv[8];
+    sum_grads8<NT, CAP>(a, world, e0, acc);
+    load_f32x8(a.master + e0, a.svec, w);
+    load_f32x8(a.m + e0, a.svec, mm);
+    load_f32x8(a.v + e0, a.svec, vv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adam_element(acc[j], a.s, w[j], mm[j], vv[j]);
+    store_f32x8(a.master + e0, a.svec, w);
+    store_f32x8(a.m + e0, a.svec, mm);
+    store_f32x8(a.v + e0, a.svec, vv);
+    store_bf16x8_rn(a.param + e0, a.pvec, w);
+  }
+  for (int64_t e = tid; e < a.head; e += nthreads) step_element<NT, CAP>(a, world, e);
+  for (int64_t e = a.head + 8 * a.nvec + tid; e < a.n; e += nthreads)
+    step_element<NT, CAP>(a, world, e);
+}
+
+// Resident blocks per SM of a kernel on the current device (cached).
+int blocks_per_sm(const void* kernel) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache[dev].find(kernel);
+  if (it != cache[dev].end()) return it->second;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess ||
+      nb < 1)
+    nb = 1;
+  cache[dev][kernel] = nb;
+  return nb;
+}
+
+// Element residue of an address within its 16-byte line.
+inline int residue(const void* p, int esize) {
+  return static_cast<int>((reinterpret_cast<uintptr_t>(p) / esize) % (16 / esize));
+}
+
+template <int NT, int CAP>
+cudaError_t launch_world(const StepLaunch& L) {
+  StepArgs<CAP> a;
+  for (int k = 0; k < L.world; ++k) a.g[k] = L.grads[k];
+  for (int k = L.world; k < CAP; ++k) a.g[k] = nullptr;
+  a.master = L.master;
+  a.m = L.m;
+  a.v = L.v;
+  a.param = L.param;
+  a.n = L.n;
+  a.world = L.world;
+  a.s = L.s;
+
+  // Pick the body's start (head in 0..7) that lets the most bytes per element
+  // move as 16-byte vectors: all gradients together (2N B), the fp32 state
+  // (24 B), the bf16 parameters (2 B).  Buffers from cudaMalloc used whole
+  // are all aligned at head = 0.
+  int rg = residue(L.grads[0], 2);
+  for (int k = 1; k < L.world; ++k)
+    if (residue(L.grads[k], 2) != rg) rg = -1;
+  int rs = residue(L.master, 4);
+  if (residue(L.m, 4) != rs || residue(L.v, 4) != rs) rs = -1;
+  const int rp = residue(L.param, 2);
+  int best_h = 0, best_score = -1;
+  for (int h = 0; h < 8; ++h) {
+    const int score = ((rg >= 0 && (rg + h) % 8 == 0) ? 2 * L.world : 0) +
+                      ((rs >= 0 && (rs + h) % 4 == 0) ? 24 : 0) + (((rp + h) % 8 == 0) ? 2 : 0);
+    if (score > best_score) {
+      best_score = score;
+      best_h = h;
+    }
+  }
+  int64_t head = best_h;
+  if (head > L.n) head = L.n;
+  a.head = static_cast<int32_t>(head);
+  a.nvec = (L.n - head) / 8;
+  a.gvec = (rg >= 0 && (rg + best_h) % 8 == 0);
+  a.svec = (rs >= 0 && (rs + best_h) % 4 == 0);
+  a.pvec = ((rp + best_h) % 8 == 0);
+
+  const void* kern = reinterpret_cast<const void*>(&zero_adam_step_kernel<NT, CAP>);
+  int sms = 0;
+  if (device_sm_count(&sms) != 0) return cudaErrorNoDevice;
+  const int64_t cap = static_cast<int64_t>(sms) * blocks_per_sm(kern);
+  int64_t blocks = (a.nvec + kThreads - 1) / kThreads;
+  if (blocks < 1) blocks = 1;
+  if (blocks > cap) blocks = cap;
+  zero_adam_step_kernel<NT, CAP><<<static_cast<unsigned>(blocks), kThreads, 0, L.stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_adam_step(const StepLaunch& L) {
+  if (L.n <= 0) return cudaSuccess;
+  (void)cudaGetLastError();  // launch errors below are this call's own
+  switch (L.world) {
+    case 1: return launch_world<1, 1>(L);
+    case 2: return launch_world<2, 2>(L);
+    case 4: return launch_world<4, 4>(L);
+    case 8: return launch_world<8, 8>(L);
+    case 16: return launch_world<16, 16>(L);
+    case 32: return launch_world<32, 32>(L);
+    case 64: return launch_world<64, 64>(L);
+    default: return launch_world<0, kTableRuntime>(L);
+  }
+}
+
+}  // namespace zeroadam

@@ -1,0 +1,258 @@
+// capi.cpp -- the extern "C" entry points of libzeroadam.so (include/zeroadam.h):
+// argument checking, the shard planner, the fp32 scalars, kernel dispatch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/zeroadam.h"
+#include "internal.h"
+
+namespace zeroadam {
+
+int device_sm_count(int* sms) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  if (dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] > 0) {
+      *sms = cache[dev];
+      return 0;
+    }
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return -1;
+  if (dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    cache[dev] = n;
+  }
+  *sms = n;
+  return 0;
+}
+
+namespace {
+
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+thread_local std::string t_msg;
+
+int launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return ZERO_OK;
+  t_last_cuda = e;
+  return e == cudaErrorNoDevice ? ZERO_E_DEVICE : ZERO_E_LAUNCH;
+}
+
+// Shard layout: ceil(numel/world) elements per rank, zero pad at the end
+// ("Implementing ZeRO's Adam from scratch": shard size and _flatten).
+int make_plan(int64_t numel, int32_t world, zero_plan_t* p) {
+  if (world < 1 || world > ZERO_MAX_WORLD) return ZERO_E_WORLD;
+  if (numel < 1) return ZERO_E_NUMEL;
+  const int64_t shard = numel / world + (numel % world != 0 ? 1 : 0);
+  if (shard > INT64_MAX / world) return ZERO_E_NUMEL;
+  const int64_t padded = shard * world;
+  // bytes_* must fit in uint64: 16*numel <= 16*INT64_MAX < 2^68 could overflow
+  if (numel > INT64_MAX / 16) return ZERO_E_NUMEL;
+  p->numel = numel;
+  p->world = world;
+  p->shard = shard;
+  p->padded = padded;
+  p->pad = padded - numel;
+  const uint64_t P = static_cast<uint64_t>(numel), S = static_cast<uint64_t>(shard);
+  // "The three stages": bf16 param (2) + bf16 grad (2) + fp32 master/m/v (12)
+  // per parameter; ZeRO-1 shards the 12, ZeRO-2 also the grad, ZeRO-3 all 16.
+  p->bytes_dp = 16 * P;
+  p->bytes_z1 = 4 * P + 12 * S;
+  p->bytes_z2 = 2 * P + 14 * S;
+  p->bytes_z3 = 16 * S;
+  const double Pd = static_cast<double>(numel), Nd = static_cast<double>(world);
+  p->formula_dp = 16.0 * Pd;
+  p->formula_z1 = 4.0 * Pd + 12.0 * Pd / Nd;
+  p->formula_z2 = 2.0 * Pd + 14.0 * Pd / Nd;
+  p->formula_z3 = 16.0 * Pd / Nd;
+  p->state_bytes_rank = 12 * S;
+  // Ring collectives over the padded bf16 vector: reduce-scatter and
+  // all-gather each send (N-1)/N of it per card.
+  const double vec_bytes = 2.0 * static_cast<double>(padded);
+  const double frac = (Nd - 1.0) / Nd;
+  p->comm_dp = 2.0 * frac * vec_bytes;
+  p->comm_z1 = p->comm_dp;
+  p->comm_z2 = p->comm_dp;
+  p->comm_z3 = 3.0 * frac * vec_bytes;
+  return ZERO_OK;
+}
+
+int check_plan(const zero_plan_t* plan) {
+  if (plan == nullptr) return ZERO_E_NULLPTR;
+  if (plan->world < 1 || plan->world > ZERO_MAX_WORLD) return ZERO_E_WORLD;
+  zero_plan_t ref;
+  const int rc = make_plan(plan->numel, static_cast<int32_t>(plan->world), &ref);
+  if (rc != ZERO_OK) return rc;
+  if (ref.shard != plan->shard || ref.pad != plan->pad || ref.padded != plan->padded)
+    return ZERO_E_PLAN;
+  return ZERO_OK;
+}
+
+bool is_finite(double x) { return std::isfinite(x); }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+Range bytes_of(const void* p, int64_t first, int64_t count, int esize) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(first) * esize;
+  return {b, b + static_cast<uintptr_t>(count) * esize};
+}
+
+}  // namespace
+}  // namespace zeroadam
+
+using namespace zeroadam;
+
+extern "C" {
+
+int zero_plan(int64_t numel, int32_t world, zero_plan_t* out) {
+  if (out == nullptr) return ZERO_E_NULLPTR;
+  return make_plan(numel, world, out);
+}
+
+int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* grad_ptrs,
+                   int32_t grad_layout, float* master, float* m, float* v, void* param_bf16,
+                   int32_t param_layout, double lr, double beta1, double beta2, double eps,
+                   int64_t t, void* stream) {
+  int rc = check_plan(plan);
+  if (rc != ZERO_OK) return rc;
+  const int32_t N = static_cast<int32_t>(plan->world);
+  if (rank != ZERO_ALL_RANKS && (rank < 0 || rank >= N)) return ZERO_E_RANK;
+  if (grad_layout != ZERO_GRAD_FULL && grad_layout != ZERO_GRAD_SHARD) return ZERO_E_LAYOUT;
+  if (param_layout != ZERO_PARAM_FULL && param_layout != ZERO_PARAM_SHARD) return ZERO_E_LAYOUT;
+  if (rank == ZERO_ALL_RANKS && (grad_layout != ZERO_GRAD_FULL || param_layout != ZERO_PARAM_FULL))
+    return ZERO_E_LAYOUT;
+  if (!is_finite(lr) || !is_finite(eps) || !is_finite(beta1) || !is_finite(beta2) || lr < 0.0 || eps < 0.0 ||
+      beta1 < 0.0 || beta1 >= 1.0 || beta2 < 0.0 || beta2 >= 1.0)
+    return ZERO_E_HPARAM;
+  if (t < 1) return ZERO_E_STEP;
+  if (grad_ptrs == nullptr || master == nullptr || m == nullptr || v == nullptr ||
+      param_bf16 == nullptr)
+    return ZERO_E_NULLPTR;
+  for (int32_t k = 0; k < N; ++k)
+    if (grad_ptrs[k] == nullptr) return ZERO_E_NULLPTR;
+
+  // The stepped range of global flat indices, clipped to the real elements.
+  int64_t lo = 0, hi = plan->numel;
+  if (rank != ZERO_ALL_RANKS) {
+    lo = static_cast<int64_t>(rank) * plan->shard;
+    hi = lo + plan->shard;
+    if (hi > plan->numel) hi = plan->numel;
+  }
+  const int64_t n = hi > lo ? hi - lo : 0;
+  // Where each buffer's element for global index lo sits.
+  const int64_t g_first = (grad_layout == ZERO_GRAD_FULL) ? lo : 0;
+  // master/m/v: all ranks' shards back to back (range starts at lo == 0), or
+  // one rank's shard (global index lo is its element 0).
+  const int64_t s_first = 0;
+  const int64_t p_first = (param_layout == ZERO_PARAM_FULL) ? lo : 0;
+
+  auto odd2 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; };
+  auto odd4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
+  if (odd4(master) || odd4(m) || odd4(v) || odd2(param_bf16)) return ZERO_E_ALIGN;
+  for (int32_t k = 0; k < N; ++k)
+    if (odd2(grad_ptrs[k])) return ZERO_E_ALIGN;
+
+  if (n > 0) {
+    const Range outs[4] = {bytes_of(master, s_first, n, 4), bytes_of(m, s_first, n, 4),
+                           bytes_of(v, s_first, n, 4), bytes_of(param_bf16, p_first, n, 2)};
+    for (int i = 0; i < 4; ++i)
+      for (int j = i + 1; j < 4; ++j)
+        if (overlap(outs[i], outs[j])) return ZERO_E_ALIAS;
+    for (int32_t k = 0; k < N; ++k) {
+      const Range g = bytes_of(grad_ptrs[k], g_first, n, 2);
+      for (int i = 0; i < 4; ++i)
+        if (overlap(g, outs[i])) return ZERO_E_ALIAS;
+    }
+  }
+  if (n == 0) return ZERO_OK;
+
+  // Offset every pointer to the range's first element.
+  const uint16_t* g[ZERO_MAX_WORLD];
+  for (int32_t k = 0; k < N; ++k) g[k] = static_cast<const uint16_t*>(grad_ptrs[k]) + g_first;
+
+  StepLaunch L;
+  L.grads = g;
+  L.world = N;
+  L.master = master + s_first;
+  L.m = m + s_first;
+  L.v = v + s_first;
+  L.param = static_cast<uint16_t*>(param_bf16) + p_first;
+  L.n = n;
+  L.stream = static_cast<cudaStream_t>(stream);
+  AdamScalars& s = L.s;
+  s.b1 = static_cast<float>(beta1);
+  s.omb1 = static_cast<float>(1.0 - beta1);
+  s.b2 = static_cast<float>(beta2);
+  s.omb2 = static_cast<float>(1.0 - beta2);
+  s.bc1 = static_cast<float>(1.0 - std::pow(beta1, static_cast<double>(t)));
+  s.bc2 = static_cast<float>(1.0 - std::pow(beta2, static_cast<double>(t)));
+  s.lr = static_cast<float>(lr);
+  s.eps = static_cast<float>(eps);
+  s.world = static_cast<float>(N);
+  s.pow2_world = (N & (N - 1)) == 0 ? 1 : 0;
+  s.inv_world = static_cast<float>(1.0 / static_cast<double>(N));
+  return launch_status(launch_adam_step(L));
+}
+
+int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs,
+                      void* full_bf16, void* stream) {
+  int rc = check_plan(unit_plan);
+  if (rc != ZERO_OK) return rc;
+  const int32_t N = static_cast<int32_t>(unit_plan->world);
+  if (shard_ptrs == nullptr || full_bf16 == nullptr) return ZERO_E_NULLPTR;
+  for (int32_t k = 0; k < N; ++k)
+    if (shard_ptrs[k] == nullptr) return ZERO_E_NULLPTR;
+  if (reinterpret_cast<uintptr_t>(full_bf16) & 1u) return ZERO_E_ALIGN;
+  for (int32_t k = 0; k < N; ++k)
+    if (reinterpret_cast<uintptr_t>(shard_ptrs[k]) & 1u) return ZERO_E_ALIGN;
+  const Range out = bytes_of(full_bf16, 0, unit_plan->numel, 2);
+  for (int32_t k = 0; k < N; ++k) {
+    int64_t cnt = unit_plan->numel - static_cast<int64_t>(k) * unit_plan->shard;
+    if (cnt > unit_plan->shard) cnt = unit_plan->shard;
+    if (cnt > 0 && overlap(out, bytes_of(shard_ptrs[k], 0, cnt, 2))) return ZERO_E_ALIAS;
+  }
+  GatherLaunch L;
+  L.shards = reinterpret_cast<const uint16_t* const*>(shard_ptrs);
+  L.world = N;
+  L.full = static_cast<uint16_t*>(full_bf16);
+  L.numel = unit_plan->numel;
+  L.shard = unit_plan->shard;
+  L.stream = static_cast<cudaStream_t>(stream);
+  return launch_status(launch_unit_gather(L));
+}
+
+const char* zero_strerror(int status) {
+  switch (status) {
+    case ZERO_OK: return "ok";
+    case ZERO_E_NULLPTR: return "a required pointer is NULL";
+    case ZERO_E_WORLD: return "world must be in [1, ZERO_MAX_WORLD]";
+    case ZERO_E_NUMEL: return "numel must be >= 1 and world*shard must fit in int64";
+    case ZERO_E_RANK: return "rank must be in [0, world) or ZERO_ALL_RANKS";
+    case ZERO_E_STEP: return "t must be >= 1 (1-based step count)";
+    case ZERO_E_ALIGN: return "bf16 pointers must be 2-byte and fp32 pointers 4-byte aligned";
+    case ZERO_E_HPARAM: return "lr and eps must be finite and >= 0, betas in [0, 1)";
+    case ZERO_E_LAYOUT: return "unknown layout, or a shard layout with ZERO_ALL_RANKS";
+    case ZERO_E_PLAN: return "plan fields differ from zero_plan(numel, world)";
+    case ZERO_E_ALIAS: return "an output buffer overlaps another buffer";
+    case ZERO_E_DEVICE: return "no usable CUDA device";
+    case ZERO_E_LAUNCH:
+      t_msg = std::string("kernel launch failed: ") + cudaGetErrorString(t_last_cuda);
+      return t_msg.c_str();
+    default: return "unknown status";
+  }
+}
+
+int zero_version(void) { return 0x000100; }
+
+}  // extern "C"

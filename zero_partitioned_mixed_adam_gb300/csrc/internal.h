@@ -1,0 +1,54 @@
+// internal.h -- declarations shared by the C-ABI layer and the kernel files of
+// libzeroadam.so.  Not installed; the public interface is include/zeroadam.h.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace zeroadam {
+
+// The step's binary32 scalars.  Each is formed in double on the host and
+// rounded to binary32 once (the page's step mixes Python floats, i.e. doubles,
+// into fp32 tensor expressions).
+struct AdamScalars {
+  float b1, omb1;    // beta1, 1 - beta1
+  float b2, omb2;    // beta2, 1 - beta2
+  float bc1, bc2;    // 1 - beta1^t, 1 - beta2^t
+  float lr, eps;
+  float world;       // N as binary32
+  float inv_world;   // 1/N, exact when N is a power of two
+  int32_t pow2_world;  // N is a power of two: g/N == g*(1/N) exactly
+};
+
+// One launch of the fused step over a contiguous range of n flat elements.
+// Every pointer already points at the range's first element.
+struct StepLaunch {
+  const uint16_t* const* grads;  // host array of `world` device pointers (bf16)
+  int32_t world;
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* param;
+  int64_t n;
+  AdamScalars s;
+  cudaStream_t stream;
+};
+
+// One launch of the ZeRO-3 unit gather.
+struct GatherLaunch {
+  const uint16_t* const* shards;  // host array of `world` device pointers (bf16)
+  int32_t world;
+  uint16_t* full;
+  int64_t numel;
+  int64_t shard;
+  cudaStream_t stream;
+};
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int device_sm_count(int* sms);
+
+cudaError_t launch_adam_step(const StepLaunch& L);
+cudaError_t launch_unit_gather(const GatherLaunch& L);
+
+}  // namespace zeroadam
