@@ -43,7 +43,9 @@ def assert_f32_close(gpu: np.ndarray, ora: np.ndarray, what: str, exact: bool = 
     nan = np.isnan(ora)
     assert (np.isnan(gpu) == nan).all(), f"{what}: NaN pattern differs"
     g, o = gpu[~nan].astype(np.float64), ora[~nan].astype(np.float64)
-    bad = np.abs(g - o) > FP32_REL * np.abs(o)
+    with np.errstate(invalid="ignore"):  # inf - inf of equal infinities is fine
+        bad = np.abs(g - o) > FP32_REL * np.abs(o)
+    bad |= np.isinf(o) & (g != o)
     if bad.any():
         i = int(np.flatnonzero(bad)[0])
         raise AssertionError(f"{what}: {int(bad.sum())} elements off by > 1e-6 relative; "

@@ -1,0 +1,131 @@
+"""ZeRO-3 unit gather and the per-unit step (through the C ABI) against the oracle.
+
+The gather is a copy, so the bar is bit-exactness.  Small cases compare the
+whole unit; the unit sweep (U up to 2^29, N in {2, 8, 64}) compares the whole
+unit with an independent device concatenation and the oracle on windows that
+cover every shard boundary.  The unit step is rank 0's step on its shard from
+N gradient slices, writing its bf16 shard.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import configs as C
+from conftest import cuda_available
+import gpu_util as gu
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
+
+import zero_partitioned_mixed_adam_gb300 as za  # noqa: E402
+
+GUARD = 256
+CANARY16 = 0x7BAD
+
+
+def _shards_dev(U, N, off=0):
+    plan = za.zero_plan(U, N)
+    bases, views = [], []
+    for r in range(N):
+        b = torch.full((plan.shard + off + GUARD,), CANARY16, dtype=torch.int16, device="cuda")
+        v = b[off:off + plan.shard]
+        gu.dev_fill_into(v, C.unit_shard_spec(U, N, r), 0, synth.OUT_BF16)
+        bases.append(b)
+        views.append(v)
+    return plan, bases, views
+
+
+def _shards_host(U, N, S):
+    return [synth.fill_host(C.unit_shard_spec(U, N, r), 0, S, synth.OUT_BF16) for r in range(N)]
+
+
+@pytest.mark.parametrize("U,N", [(1, 1), (1, 4), (7, 3), (8, 8), (100, 9), (1001, 3), (4096, 2),
+                                 (65537, 8), (100_000, 64), (123_457, 65), (1 << 20, 64)])
+def test_gather_small_whole_unit(U, N):
+    plan, bases, shards = _shards_dev(U, N)
+    fb = torch.full((U + 2 * GUARD,), CANARY16, dtype=torch.int16, device="cuda")
+    full = fb[GUARD:GUARD + U]
+    za.zero3_unit_gather(plan, shards, full)
+    torch.cuda.synchronize()
+    ref = oracle.unit_gather(U, N, _shards_host(U, N, plan.shard))
+    assert (gu.to_host_u16(full) == ref).all()
+    assert bool((fb[:GUARD] == CANARY16).all()) and bool((fb[GUARD + U:] == CANARY16).all())
+
+
+@pytest.mark.parametrize("off_src,off_dst", [(1, 0), (0, 1), (3, 5), (4, 4)])
+def test_gather_misaligned(off_src, off_dst):
+    U, N = 50_001, 4
+    plan, bases, shards = _shards_dev(U, N, off=off_src)
+    fb = torch.full((U + off_dst + GUARD,), CANARY16, dtype=torch.int16, device="cuda")
+    full = fb[off_dst:off_dst + U]
+    za.zero3_unit_gather(plan, shards, full)
+    torch.cuda.synchronize()
+    ref = oracle.unit_gather(U, N, _shards_host(U, N, plan.shard))
+    assert (gu.to_host_u16(full) == ref).all()
+    assert bool((fb[:off_dst] == CANARY16).all()) and bool((fb[off_dst + U:] == CANARY16).all())
+
+
+@pytest.mark.parametrize("U", C.UNIT_SIZES)
+@pytest.mark.parametrize("N", C.UNIT_WORLDS)
+def test_unit_sweep_gather_and_step(U, N):
+    """The sweep's configuration: gather the N parameter shards, then rank 0's step on
+    its shard from N gradient slices (ZERO_GRAD_SHARD, ZERO_PARAM_SHARD)."""
+    plan, bases, shards = _shards_dev(U, N)
+    S = plan.shard
+    full = torch.empty(U, dtype=torch.int16, device="cuda")
+    za.zero3_unit_gather(plan, shards, full)
+    # an independent device concatenation (torch) of the same shards
+    cat = torch.cat(shards)[:U]
+    assert torch.equal(full, cat)
+    # the oracle on windows around every shard boundary and at both ends
+    torch.cuda.synchronize()
+    wins = [(0, min(U, 64)), (max(0, U - 64), U)]
+    for r in range(1, N):
+        b = r * S
+        if b < U:
+            wins.append((b - 8, min(U, b + 8)))
+    host_sh = [synth.fill_host(C.unit_shard_spec(U, N, r), 0, S, synth.OUT_BF16) for r in range(N)] \
+        if U * 1 <= (1 << 24) else None
+    if host_sh is not None:
+        ref = oracle.unit_gather(U, N, host_sh)
+        assert (gu.to_host_u16(full) == ref).all()
+    else:
+        for a, b in wins:
+            # element i of the unit comes from shard i // S at i % S
+            exp = np.array([synth.fill_host(C.unit_shard_spec(U, N, i // S), i % S, 1,
+                                            synth.OUT_BF16)[0] for i in range(a, b)], np.uint16)
+            assert (gu.to_host_u16(full[a:b]) == exp).all(), (a, b)
+    del full, cat, bases, shards
+
+    # rank 0's step on its shard
+    wl = C.unit_workload(U, N)
+    g = [torch.empty(S, dtype=torch.int16, device="cuda") for _ in range(N)]
+    for k in range(N):
+        gu.dev_fill_into(g[k], wl.grad_spec(k, 1), 0, synth.OUT_BF16)
+    w = torch.empty(S, dtype=torch.float32, device="cuda")
+    gu.dev_fill_into(w, wl.master_spec(), 0, synth.OUT_F32)
+    m = torch.zeros_like(w)
+    v = torch.zeros_like(w)
+    p = torch.full((S,), 0x1234, dtype=torch.int16, device="cuda")
+    za.zero_adam_step(plan, 0, g, w, m, v, p, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                      eps=wl.eps, t=1, grad_layout=za.ZERO_GRAD_SHARD,
+                      param_layout=za.ZERO_PARAM_SHARD)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(U + N)
+    for a in sorted({0, max(0, S - 1024), int(rng.integers(0, max(1, S - 1024)))}):
+        b = min(S, a + 1024)
+        hg = [synth.fill_host(wl.grad_spec(k, 1), a, b - a, synth.OUT_BF16) for k in range(N)]
+        hw = synth.fill_host(wl.master_spec(), a, b - a, synth.OUT_F32)
+        hm = np.zeros(b - a, np.float32)
+        hv = np.zeros(b - a, np.float32)
+        hp = np.zeros(b - a, np.uint16)
+        oracle.zero_step(U, N, 0, hg, hw, hm, hv, hp, wl.lr, wl.beta1, wl.beta2, wl.eps, 1,
+                         i0=a, i1=b, grad_base=a, state_base=a, param_base=a)
+        gu.assert_f32_close(gu.to_host_f32(w[a:b]), hw, f"unit {U}/{N} master [{a},{b})")
+        gu.assert_f32_close(gu.to_host_f32(m[a:b]), hm, f"unit {U}/{N} m [{a},{b})")
+        gu.assert_f32_close(gu.to_host_f32(v[a:b]), hv, f"unit {U}/{N} v [{a},{b})")
+        gu.assert_bf16_close(gu.to_host_u16(p[a:b]), hp, f"unit {U}/{N} param [{a},{b})")
+    del g, w, m, v, p
+    torch.cuda.empty_cache()

@@ -292,8 +292,11 @@ def test_gpt2_small_ten_steps_every_element():
             gu.spot_check_generated(hg[k][:numel], wl.grad_spec(k, t), 0, synth.OUT_BF16,
                                     samples=512, seed=t * 100 + k)
         if t == 1:
-            zero = (hg[0][:numel] == 0)
-            assert abs(zero.mean() - 0.1) < 0.01 and (hg[5][:numel][zero] == 0).all()
+            # the 10 % zero mask is shared by the ranks; outside it a draw is exactly 0
+            # only when the polar method's uniform hits 1/2 exactly (2^-24 per element)
+            z0, z5 = hg[0][:numel] == 0, hg[5][:numel] == 0
+            assert abs((z0 & z5).mean() - 0.1) < 0.01
+            assert (z0 ^ z5).mean() < 1e-6
         gu.oracle_step_parallel(numel, world, -1, hg, hw, hm, hv, hp, wl.lr, wl.beta1, wl.beta2,
                                 wl.eps, t)
         gu.assert_f32_close(gu.to_host_f32(w)[:numel], hw[:numel], f"gpt2 master t={t}")
