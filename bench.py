@@ -141,45 +141,87 @@ def _traffic_record(kernel_src):
         return None
 
 
-def _alloc_workload(wl, dev):
-    """Device buffers of one replica, filled by the seeded generator."""
-    import torch
-    import synth
-    import zero_partitioned_mixed_adam_gb300 as za
-    plan = za.zero_plan(wl.numel, wl.world)
-    S, P = plan.shard, plan.padded
-    single = wl.rank >= 0
-    lo = wl.rank * S if single else 0
-    n = _elements(wl, plan)
-    g_len = S if wl.grad_layout == "shard" else P
-    s_len = S if single else P
-    p_len = S if wl.param_layout == "shard" else wl.numel
-    g = [torch.zeros(g_len, dtype=torch.int16, device=dev) for _ in range(wl.world)]
-    w = torch.zeros(s_len, dtype=torch.float32, device=dev)
-    m = torch.zeros_like(w)
-    v = torch.zeros_like(w)
-    p = torch.zeros(p_len, dtype=torch.int16, device=dev)
-    st = torch.cuda.current_stream(dev).cuda_stream
-    synth.fill_dev(wl.master_spec(), lo, n, synth.OUT_F32, w.data_ptr(), st)
-    return plan, g, w, m, v, p, lo, n
+class Replica:
+    """One replica's device buffers and the launches of one step.
 
+    Step workloads: one zero_adam_step.  Unit workloads (ZeRO-3): the unit
+    gather of the N parameter shards, then rank 0's step on its shard."""
 
-def _fill_grads(wl, g, lo, n, t, dev):
-    import torch
-    import synth
-    st = torch.cuda.current_stream(dev).cuda_stream
-    g_first = 0 if wl.grad_layout == "shard" else lo
-    for k in range(wl.world):
-        synth.fill_dev(wl.grad_spec(k, t), lo, n, synth.OUT_BF16,
-                       g[k].data_ptr() + 2 * g_first, st)
+    def __init__(self, wl, dev):
+        import torch
+        import synth
+        import zero_partitioned_mixed_adam_gb300 as za
+        self.za, self.wl, self.dev = za, wl, dev
+        self.plan = plan = za.zero_plan(wl.numel, wl.world)
+        S, P = plan.shard, plan.padded
+        single = wl.rank >= 0
+        self.lo = wl.rank * S if single else 0
+        self.n = n = _elements(wl, plan)
+        self.unit = wl.name.startswith("unit")
+        g_len = S if wl.grad_layout == "shard" else P
+        s_len = S if single else P
+        p_len = S if wl.param_layout == "shard" else wl.numel
+        self.g_first = 0 if wl.grad_layout == "shard" else self.lo
+        self.p_first = 0 if wl.param_layout == "shard" else self.lo
+        self.g = [torch.zeros(g_len, dtype=torch.int16, device=dev) for _ in range(wl.world)]
+        self.w = torch.zeros(s_len, dtype=torch.float32, device=dev)
+        self.m = torch.zeros_like(self.w)
+        self.v = torch.zeros_like(self.w)
+        self.p = torch.zeros(p_len, dtype=torch.int16, device=dev)
+        st = torch.cuda.current_stream(dev).cuda_stream
+        synth.fill_dev(wl.master_spec(), self.lo, n, synth.OUT_F32, self.w.data_ptr(), st)
+        self.shards, self.full = None, None
+        if self.unit:
+            from synth import configs as C
+            self.shards = [torch.empty(S, dtype=torch.int16, device=dev) for _ in range(wl.world)]
+            for r in range(wl.world):
+                synth.fill_dev(C.unit_shard_spec(wl.numel, wl.world, r), 0, S, synth.OUT_BF16,
+                               self.shards[r].data_ptr(), st)
+            self.full = torch.empty(wl.numel, dtype=torch.int16, device=dev)
+        # (name, algorithmic bytes) of the step's launches, in order
+        self.kernels = []
+        if self.unit:
+            self.kernels.append(("zero3_unit_gather_kernel", 4 * wl.numel))
+        self.kernels.append(("zero_adam_step_kernel", _bytes_per_step(wl, plan)))
 
+    def fill_grads(self, t):
+        import torch
+        import synth
+        st = torch.cuda.current_stream(self.dev).cuda_stream
+        for k in range(self.wl.world):
+            synth.fill_dev(self.wl.grad_spec(k, t), self.lo, self.n, synth.OUT_BF16,
+                           self.g[k].data_ptr() + 2 * self.g_first, st)
 
-def _step(za, wl, plan, g, w, m, v, p, t, stream):
-    za.zero_adam_step(plan, wl.rank, g, w, m, v, p, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
-                      eps=wl.eps, t=t,
-                      grad_layout=za.ZERO_GRAD_SHARD if wl.grad_layout == "shard" else 0,
-                      param_layout=za.ZERO_PARAM_SHARD if wl.param_layout == "shard" else 0,
-                      stream=stream)
+    def step(self, t, stream, ev=None, grads=None, shards=None, param=None):
+        """Issue one step; ev[i] = (start, end) events around launch i when given.
+        grads/shards/param override the device buffers (host-resident inputs)."""
+        za, wl = self.za, self.wl
+        i = 0
+        if self.unit:
+            if ev is not None:
+                ev[i][0].record(stream)
+            za.zero3_unit_gather(self.plan, shards or self.shards, self.full, stream=stream)
+            if ev is not None:
+                ev[i][1].record(stream)
+            i += 1
+        if ev is not None:
+            ev[i][0].record(stream)
+        za.zero_adam_step(self.plan, wl.rank, grads or self.g, self.w, self.m, self.v,
+                          param if param is not None else self.p, lr=wl.lr, beta1=wl.beta1,
+                          beta2=wl.beta2, eps=wl.eps, t=t,
+                          grad_layout=za.ZERO_GRAD_SHARD if wl.grad_layout == "shard" else 0,
+                          param_layout=za.ZERO_PARAM_SHARD if wl.param_layout == "shard" else 0,
+                          stream=stream)
+        if ev is not None:
+            ev[i][1].record(stream)
+
+    def unit_elements(self):
+        """Elements one step processes: the unit's U for ZeRO-3 units, else the
+        stepped parameters."""
+        return self.wl.numel if self.unit else self.n
+
+    def step_bytes(self):
+        return sum(b for _, b in self.kernels)
 
 
 class OracleSample:
@@ -288,15 +330,19 @@ def aggregate(ms_local: float, elems_per_rank: int, world_size: int, dist=None, 
     return ms, world_size * elems_per_rank / (ms * 1e-3) / 1e9
 
 
-def _config(wl, plan):
+def _config(wl, rep):
     c = {"workload": wl.name, "numel": wl.numel, "world": wl.world,
          "rank": "all" if wl.rank < 0 else wl.rank, "grad_layout": wl.grad_layout,
          "param_layout": wl.param_layout, "grad_dist": ["normal", "student_t3"][wl.grad_dist],
          "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas",
          "state": "fp32 master/m/v, bf16 grads and params"}
-    if plan is not None:
-        c["shard"] = plan.shard
-        c["bytes_per_step"] = _bytes_per_step(wl, plan)
+    if rep is not None:
+        c["shard"] = rep.plan.shard
+        c["bytes_per_step"] = rep.step_bytes()
+        c["launches_per_step"] = [k for k, _ in rep.kernels]
+        if rep.unit:
+            c["unit_step"] = "zero3_unit_gather of the N shards + rank 0's step on its shard"
+            c["elements"] = "unit elements U per step"
     return c
 
 
@@ -312,23 +358,23 @@ def run_ours(args, wl):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    import zero_partitioned_mixed_adam_gb300 as za
 
-    plan, g, w, m, v, p, lo, n = _alloc_workload(wl, dev)
+    rep = Replica(wl, dev)
     stream = torch.cuda.current_stream(dev)
     # prewarm steps (state as after t = 1..prewarm), then the timed gradients
     t = 0
     for t in range(1, wl.prewarm + 1):
-        _fill_grads(wl, g, lo, n, t, dev)
-        _step(za, wl, plan, g, w, m, v, p, t, stream)
-    _fill_grads(wl, g, lo, n, wl.prewarm + 1, dev)
+        rep.fill_grads(t)
+        rep.step(t, stream)
+    rep.fill_grads(wl.prewarm + 1)
     for _ in range(args.warmup):
         t += 1
-        _step(za, wl, plan, g, w, m, v, p, t, stream)
+        rep.step(t, stream)
     torch.cuda.synchronize(dev)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    nk = len(rep.kernels)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nk)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     if dist is not None:
@@ -337,51 +383,56 @@ def run_ours(args, wl):
     t_wall = time.perf_counter()
     for i in range(args.steps):
         t += 1
-        ev[i][0].record(stream)
-        _step(za, wl, plan, g, w, m, v, p, t, stream)
-        ev[i][1].record(stream)
+        rep.step(t, stream, ev[i])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t_wall
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = ev[0][0].elapsed_time(ev[-1][1])
-    elems = _elements(wl, plan)
-    bytes_step = _bytes_per_step(wl, plan)
+    total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1])
+    per_kernel = []
+    for j, (name, nbytes) in enumerate(rep.kernels):
+        ms = [ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps)]
+        per_kernel.append({"kernel": name, "algorithmic_bytes_per_launch": nbytes,
+                           "avg_launch_ms": statistics.mean(ms),
+                           "median_launch_ms": statistics.median(ms),
+                           "gbs": nbytes / (statistics.mean(ms) * 1e-3) / 1e9})
+    elems = rep.unit_elements()
     ms_step, value = aggregate(total_ms / args.steps, elems, world_size, dist, dev)
-    avg_launch_ms = statistics.mean(launch_ms)
-    achieved = bytes_step / (avg_launch_ms * 1e-3) / 1e9
+    dom = max(per_kernel, key=lambda k: k["avg_launch_ms"] * 1)
     peak, peak_src = _peaks()
     traffic = None
-    rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc",
-                                       "adam_step.cu"))
-    if rec and rec.get("world") == wl.world:
-        traffic = rec["dram_bytes_per_element"] * elems
+    if dom["kernel"] == "zero_adam_step_kernel":
+        rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc",
+                                           "adam_step.cu"))
+        if rec and rec.get("world") == wl.world:
+            traffic = rec["dram_bytes_per_element"] * rep.n
 
     e2e = None
     cpu = None
     if not args.no_e2e:
-        e2e = _e2e(args, wl, za, plan, g, w, m, v, p, lo, n, dev, stream, t, dist, world_size)
+        e2e = _e2e(args, rep, stream, t, dist, world_size)
         t += e2e.pop("_steps")
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
         cpu = _cpu_oracle_sample(wl, args.cpu_seconds)
 
     if rank == 0:
+        step_gbs = rep.step_bytes() / (ms_step * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": world_size,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": _config(wl, plan),
-            "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
+            "data": "synthetic", "config": _config(wl, rep),
+            "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak,
+            "roofline": {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": dom["gbs"] / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-                         "kernel": "zero_adam_step_kernel",
-                         "algorithmic_bytes_per_launch": bytes_step,
-                         "avg_launch_ms": avg_launch_ms,
-                         "median_launch_ms": statistics.median(launch_ms)},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+                         "kernel": dom["kernel"],
+                         "algorithmic_bytes_per_launch": dom["algorithmic_bytes_per_launch"],
+                         "avg_launch_ms": dom["avg_launch_ms"],
+                         "median_launch_ms": dom["median_launch_ms"]},
+            "kernels": per_kernel,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * nk,
             "clocks": clocks, "wall_s_timed": wall,
         }
         print(json.dumps(line), flush=True)
@@ -390,44 +441,73 @@ def run_ours(args, wl):
     return 0
 
 
-def _e2e(args, wl, za, plan, g, w, m, v, p, lo, n, dev, stream, t, dist, world_size):
-    """The same step through the public API with host buffers: every step copies the
-    N ranks' gradients from pinned host memory, steps, and reads the bf16
-    parameters back, all inside the timed region."""
+def _e2e(args, rep, stream, t, dist, world_size):
+    """The same step through the public API with HOST buffers.  Every step's inputs
+    (the N ranks' gradients; for ZeRO-3 units also the N parameter shards) sit in
+    pinned host memory and its result (the bf16 parameters of the stepped range) is
+    written to pinned host memory.  The fused kernel reads the host gradients
+    directly over NVLink-C2C and writes the host parameters (no staging copies),
+    so every byte crosses the host link inside the timed region.  The copy-engine
+    alternative (cudaMemcpyAsync in, step, out) is timed too and reported beside."""
     import torch
+    wl = rep.wl
     k_steps = max(1, min(args.steps, args.e2e_steps))
-    g_first = 0 if wl.grad_layout == "shard" else lo
-    hg = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(wl.world)]
+    n = rep.n
+    g_len = rep.g[0].numel()
+    hg = [torch.empty(g_len, dtype=torch.int16, pin_memory=True) for _ in range(wl.world)]
     for k in range(wl.world):
-        hg[k].copy_(g[k][g_first:g_first + n])
-    p_first = 0 if wl.param_layout == "shard" else lo
-    hp = torch.empty(n, dtype=torch.int16, pin_memory=True)
-    torch.cuda.synchronize(dev)
+        hg[k].copy_(rep.g[k])
+    hs = None
+    if rep.unit:
+        hs = [torch.empty(sk.numel(), dtype=torch.int16, pin_memory=True) for sk in rep.shards]
+        for hsk, sk in zip(hs, rep.shards):
+            hsk.copy_(sk)
+    hp = torch.empty(rep.p.numel(), dtype=torch.int16, pin_memory=True)
+    torch.cuda.synchronize(rep.dev)
+    in_bytes = sum(x.numel() * 2 for x in hg)
+    if rep.unit:
+        in_bytes = 2 * n * wl.world + sum(x.numel() * 2 for x in hs)
+    elif wl.grad_layout != "shard":
+        in_bytes = 2 * n * wl.world   # the kernel reads the stepped range only
 
-    def one(tt):
+    def zero_copy(tt):
+        rep.step(tt, stream, grads=hg, shards=hs, param=hp)
+
+    def copies(tt):
         for k in range(wl.world):
-            g[k][g_first:g_first + n].copy_(hg[k], non_blocking=True)
-        _step(za, wl, plan, g, w, m, v, p, tt, stream)
-        hp.copy_(p[p_first:p_first + n], non_blocking=True)
+            rep.g[k].copy_(hg[k], non_blocking=True)
+        if rep.unit:
+            for sk, hsk in zip(rep.shards, hs):
+                sk.copy_(hsk, non_blocking=True)
+        rep.step(tt, stream)
+        hp.copy_(rep.p, non_blocking=True)
 
-    t += 1
-    one(t)  # warm-up
-    torch.cuda.synchronize(dev)
-    if dist is not None:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(k_steps):
+    out = {}
+    for name, fn in (("zero_copy", zero_copy), ("copy_engine", copies)):
         t += 1
-        one(t)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    elems = _elements(wl, plan)
-    ms, val = aggregate(e0.elapsed_time(e1) / k_steps, elems, world_size, dist, dev)
+        fn(t)  # warm-up
+        torch.cuda.synchronize(rep.dev)
+        if dist is not None:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_steps):
+            t += 1
+            fn(t)
+        e1.record(stream)
+        torch.cuda.synchronize(rep.dev)
+        out[name] = aggregate(e0.elapsed_time(e1) / k_steps, rep.unit_elements(), world_size,
+                              dist, rep.dev)
+    ms, val = out["zero_copy"]
     return {"value": val, "unit": "Gelem/s",
-            "h2d_bytes_per_step": 2 * n * wl.world, "d2h_bytes_per_step": 2 * n,
-            "ms_per_step": ms, "steps": k_steps, "_steps": k_steps + 1}
+            "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 2 * n,
+            "ms_per_step": ms, "steps": k_steps,
+            "mode": "zero-copy: the kernel reads pinned host inputs and writes pinned host "
+                    "parameters over NVLink-C2C",
+            "copy_engine": {"value": out["copy_engine"][1], "ms_per_step": out["copy_engine"][0],
+                            "mode": "cudaMemcpyAsync H2D, step, D2H on one stream"},
+            "_steps": 2 * (k_steps + 1)}
 
 
 def main(argv=None):

@@ -55,6 +55,7 @@ extern "C" {
 #define ZERO_E_ALIAS (-10)  /* an output buffer overlaps another buffer             */
 #define ZERO_E_LAUNCH (-11) /* the CUDA launch failed; see zero_strerror            */
 #define ZERO_E_DEVICE (-12) /* no usable CUDA device                                */
+#define ZERO_E_RANGE (-13)  /* zero_adam_step_range: begin < 0 or end < begin       */
 
 /* Largest world (number of emulated data-parallel ranks) accepted. */
 #define ZERO_MAX_WORLD 1024
@@ -62,9 +63,13 @@ extern "C" {
 /* rank argument: step every rank's shard in one launch. */
 #define ZERO_ALL_RANKS (-1)
 
-/* grad_layout */
-#define ZERO_GRAD_FULL 0  /* grad_ptrs[k]: rank k's whole padded flat gradient (>= numel elements) */
-#define ZERO_GRAD_SHARD 1 /* grad_ptrs[k]: rank k's gradient slice of THIS rank's shard (shard elements); single rank only */
+/* grad_layout: one layout, optionally OR-ed with the flags below */
+#define ZERO_GRAD_FULL 0   /* grad_ptrs[k]: rank k's whole padded flat gradient (>= numel elements) */
+#define ZERO_GRAD_SHARD 1  /* grad_ptrs[k]: rank k's gradient slice of THIS rank's shard (shard elements); single rank only */
+#define ZERO_GRAD_WINDOW 2 /* zero_adam_step_range only: grad_ptrs[k][i - begin], the window's gradients alone */
+#define ZERO_GRAD_LAYOUT_MASK 0x0f
+#define ZERO_GRAD_F32 0x10 /* flag: gradient buffers hold fp32 (default: bf16) */
+#define ZERO_ACC_BF16 0x20 /* flag: round the running sum over ranks to bf16 after every addition */
 
 /* param_layout */
 #define ZERO_PARAM_FULL 0  /* param_bf16: the whole flat parameter buffer (>= numel elements) */
@@ -127,9 +132,10 @@ int zero_plan(int64_t numel, int32_t world, zero_plan_t* out);
  *
  *   plan        from zero_plan(numel, world); checked (ZERO_E_PLAN).
  *   rank        in [0, world), or ZERO_ALL_RANKS.
- *   grad_ptrs   host array of world device pointers, bf16.
+ *   grad_ptrs   host array of world device pointers, bf16 (fp32 with ZERO_GRAD_F32).
  *               ZERO_GRAD_FULL : grad_ptrs[k][i] for global index i.
  *               ZERO_GRAD_SHARD: grad_ptrs[k][i - rank*shard] (single rank).
+ *               (ZERO_GRAD_WINDOW is zero_adam_step_range's; here ZERO_E_LAYOUT.)
  *   master,m,v  device fp32, read and written in place.
  *               ALL_RANKS: padded elements, index i (the ranks' shards back to
  *               back); single rank: shard elements, index i - rank*shard.
@@ -147,6 +153,30 @@ int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* gra
                    int32_t grad_layout, float* master, float* m, float* v, void* param_bf16,
                    int32_t param_layout, double lr, double beta1, double beta2, double eps,
                    int64_t t, void* stream);
+
+/*
+ * The same step restricted to the global flat window [begin, end) (clipped to
+ * the stepped rank's real elements): ZeRO-2's bucketed schedule ("Implementing
+ * ZeRO's Adam from scratch", closing note: real ZeRO-2 reduce-scatters bucket
+ * by bucket during the backward pass and frees each full-gradient bucket once
+ * it has gone out).  With ZERO_GRAD_WINDOW each grad_ptrs[k] holds only the
+ * bucket, element i at grad_ptrs[k][i - begin], so the full gradient never
+ * needs to exist; ZERO_GRAD_FULL and ZERO_GRAD_SHARD address as in
+ * zero_adam_step.  master/m/v and param_bf16 are addressed as in
+ * zero_adam_step.  Buckets that tile the flat vector give exactly the result
+ * of one zero_adam_step (the step is elementwise).  Errors: those of
+ * zero_adam_step, and ZERO_E_RANGE.
+ *
+ * Gradient variants (flags in grad_layout, both calls): ZERO_GRAD_F32 takes
+ * fp32 gradient buffers (the page's runnable demo keeps fp32 gradients);
+ * ZERO_ACC_BF16 rounds the running sum over ranks to bf16 after every
+ * addition, the result a reduce-scatter on bf16 buffers delivers (a
+ * sensitivity variant, not the method).
+ */
+int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end,
+                         const void* const* grad_ptrs, int32_t grad_layout, float* master,
+                         float* m, float* v, void* param_bf16, int32_t param_layout, double lr,
+                         double beta1, double beta2, double eps, int64_t t, void* stream);
 
 /* ------------------------------------------------------------ ZeRO-3 gather */
 

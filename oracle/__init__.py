@@ -35,6 +35,8 @@ class _Plan(ctypes.Structure):
         ("formula_dp", ctypes.c_double), ("formula_z1", ctypes.c_double),
         ("formula_z2", ctypes.c_double), ("formula_z3", ctypes.c_double),
         ("state_bytes_rank", ctypes.c_uint64),
+        ("comm_dp", ctypes.c_double), ("comm_z1", ctypes.c_double),
+        ("comm_z2", ctypes.c_double), ("comm_z3", ctypes.c_double),
     ]
 
 
@@ -82,6 +84,12 @@ def _L():
              ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
              ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_double] * 4 + [ctypes.c_int64])
         lib.oracle_zero_step.restype = ctypes.c_int
+        lib.oracle_zero_step_ex.argtypes = (
+            [P(_Plan), ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+             ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64]
+            + [ctypes.c_double] * 4 + [ctypes.c_int64])
+        lib.oracle_zero_step_ex.restype = ctypes.c_int
         lib.oracle_dp_step.argtypes = (
             [ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
              ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_double] * 4 + [ctypes.c_int64])
@@ -97,9 +105,9 @@ def _ptr(a: np.ndarray) -> ctypes.c_void_p:
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _ptr_array(arrs) -> ctypes.Array:
+def _ptr_array(arrs, dtype=np.uint16) -> ctypes.Array:
     for a in arrs:
-        assert a.dtype == np.uint16 and a.flags.c_contiguous
+        assert a.dtype == dtype and a.flags.c_contiguous
     return (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
 
 
@@ -138,11 +146,14 @@ def scalars(lr, beta1, beta2, eps, t, world) -> dict:
 
 
 def zero_step(numel, world, rank, grads, master, m, v, param, lr, beta1, beta2, eps, t, *,
-              i0=0, i1=None, grad_base=0, state_base=0, param_base=0) -> None:
+              i0=0, i1=None, grad_base=0, state_base=0, param_base=0, grad_f32=False,
+              acc_bf16=False) -> None:
     """ZeroAdam.step for one rank (rank >= 0) or all ranks (rank = -1), in place.
 
     Arrays are addressed by global flat index minus their base (see
-    oracle_zero_step); only global indices in [i0, i1) are touched.
+    oracle_zero_step); only global indices in [i0, i1) are touched.  grads are
+    uint16 (bf16 bits), or float32 with grad_f32; acc_bf16 selects the
+    bf16-rounded running sum (a variant, not the method).
     """
     p = _plan_struct(numel, world)
     if i1 is None:
@@ -151,10 +162,16 @@ def zero_step(numel, world, rank, grads, master, m, v, param, lr, beta1, beta2, 
     for a in (master, m, v):
         assert a.dtype == np.float32 and a.flags.c_contiguous
     assert param.dtype == np.uint16 and param.flags.c_contiguous
-    ptrs = _ptr_array(grads)
-    rc = _L().oracle_zero_step(ctypes.byref(p), rank, i0, i1, ptrs, grad_base, _ptr(master),
-                               _ptr(m), _ptr(v), state_base, _ptr(param), param_base,
-                               lr, beta1, beta2, eps, t)
+    ptrs = _ptr_array(grads, np.float32 if grad_f32 else np.uint16)
+    if not grad_f32 and not acc_bf16:
+        rc = _L().oracle_zero_step(ctypes.byref(p), rank, i0, i1, ptrs, grad_base, _ptr(master),
+                                   _ptr(m), _ptr(v), state_base, _ptr(param), param_base,
+                                   lr, beta1, beta2, eps, t)
+    else:
+        rc = _L().oracle_zero_step_ex(ctypes.byref(p), rank, i0, i1, ptrs, grad_base,
+                                      int(grad_f32), int(acc_bf16), _ptr(master), _ptr(m),
+                                      _ptr(v), state_base, _ptr(param), param_base,
+                                      lr, beta1, beta2, eps, t)
     if rc != 0:
         raise ValueError(f"oracle_zero_step failed ({rc})")
 

@@ -91,6 +91,25 @@ int oracle_plan(int64_t numel, int32_t world, oracle_plan_t* out) {
   out->formula_z3 = 16.0 * P / N;
   /* ZeroAdam.state_bytes: master + m + v of this rank, fp32 */
   out->state_bytes_rank = 3u * 4u * (uint64_t)shard;
+
+  /*
+   * Bytes each card sends per step ("The three stages" table, last column;
+   * "Exercises", second answer).  The collectives run on the padded bf16
+   * vector (2 bytes x padded).  In a ring, a reduce-scatter and an all-gather
+   * each send (N-1)/N of the vector per card, and an all-reduce is one of
+   * each.  DP all-reduces the gradients; ZeRO-1 and ZeRO-2 reduce-scatter the
+   * gradients and all-gather the parameters; ZeRO-3 all-gathers the
+   * parameters in the forward and again in the backward pass and
+   * reduce-scatters the gradients.
+   */
+  const double vec = 2.0 * (double)out->padded;
+  const double ring_share = ((double)world - 1.0) / (double)world;
+  const double reduce_scatter = ring_share * vec;
+  const double all_gather = ring_share * vec;
+  out->comm_dp = reduce_scatter + all_gather;
+  out->comm_z1 = reduce_scatter + all_gather;
+  out->comm_z2 = reduce_scatter + all_gather;
+  out->comm_z3 = all_gather + all_gather + reduce_scatter;
   return 0;
 }
 
@@ -145,11 +164,32 @@ void oracle_scalars(double lr, double beta1, double beta2, double eps, int64_t t
 
 /* ------------------------------------------------------------ one element */
 
+/* Rank k's gradient at buffer index idx, widened to fp32 (exact). */
+static float oracle_grad(const void* const* grads, int grad_f32, int32_t k, int64_t idx) {
+  if (grad_f32) return ((const float*)grads[k])[idx];
+  return oracle_bf16_to_f32(((const uint16_t*)grads[k])[idx]);
+}
+
 /*
- * One flat element of ZeroAdam.step, in the page's order:
- *   reduce_scatter_tensor     g  = g_0 + g_1 + ... + g_{N-1}   (ranks in order,
- *                                                              fp32 accumulator
- *                                                              starting at g_0)
+ * reduce_scatter_tensor of one element: the ranks' gradients summed in rank
+ * order 0..N-1 in fp32, starting from rank 0's value.  Variant (not the
+ * method): acc_bf16 rounds every partial sum to bf16, what a reduce-scatter
+ * on bf16 buffers delivers.
+ */
+static float oracle_reduce(const void* const* grads, int grad_f32, int acc_bf16, int32_t world,
+                           int64_t idx) {
+  float acc = oracle_grad(grads, grad_f32, 0, idx);
+  if (acc_bf16) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(acc));
+  for (int32_t k = 1; k < world; ++k) {
+    acc = acc + oracle_grad(grads, grad_f32, k, idx);
+    if (acc_bf16) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(acc));
+  }
+  return acc;
+}
+
+/*
+ * One flat element of ZeroAdam.step, in the page's order, from the summed
+ * gradient acc:
  *   g /= world                g  = g / N
  *   m.mul_(b1).add_(g, alpha=1-b1)           m = m*b1 + (1-b1)*g
  *   v.mul_(b2).addcmul_(g, g, value=1-b2)    v = v*b2 + ((1-b2)*g)*g
@@ -157,12 +197,9 @@ void oracle_scalars(double lr, double beta1, double beta2, double eps, int64_t t
  *   master -= lr * m_hat / (v_hat.sqrt() + eps)
  *                                            w = w - (lr*m_hat) / (sqrt(v_hat)+eps)
  *   all_gather + copy into p.data            p = bf16(w)  (bf16 parameters)
- * gk[k] is rank k's bf16 gradient of this element.
  */
-static void oracle_adam_element(const uint16_t* gk, int32_t world, const oracle_scalars_t* s,
-                                float* w, float* m, float* v, uint16_t* p) {
-  float acc = oracle_bf16_to_f32(gk[0]);
-  for (int32_t k = 1; k < world; ++k) acc = acc + oracle_bf16_to_f32(gk[k]);
+static void oracle_adam_element(float acc, const oracle_scalars_t* s, float* w, float* m,
+                                float* v, uint16_t* p) {
   const float g = acc / s->world;
 
   float mm = *m, vv = *v, ww = *w;
@@ -199,10 +236,11 @@ static void oracle_adam_element(const uint16_t* gk, int32_t world, const oracle_
  * dropped when the gathered vector is copied back into the parameters.  The
  * oracle therefore neither reads nor writes any index >= numel.
  */
-int oracle_zero_step(const oracle_plan_t* plan, int32_t rank, int64_t i0, int64_t i1,
-                     const uint16_t* const* grads, int64_t grad_base, float* master, float* m,
-                     float* v, int64_t state_base, uint16_t* param, int64_t param_base, double lr,
-                     double beta1, double beta2, double eps, int64_t t) {
+int oracle_zero_step_ex(const oracle_plan_t* plan, int32_t rank, int64_t i0, int64_t i1,
+                        const void* const* grads, int64_t grad_base, int grad_f32, int acc_bf16,
+                        float* master, float* m, float* v, int64_t state_base, uint16_t* param,
+                        int64_t param_base, double lr, double beta1, double beta2, double eps,
+                        int64_t t) {
   if (plan == NULL || grads == NULL || master == NULL || m == NULL || v == NULL || param == NULL)
     return -1;
   if (t < 1 || rank >= plan->world || plan->world > ORACLE_MAX_WORLD) return -1;
@@ -211,7 +249,6 @@ int oracle_zero_step(const oracle_plan_t* plan, int32_t rank, int64_t i0, int64_
 
   const int32_t r_first = rank < 0 ? 0 : rank;
   const int32_t r_last = rank < 0 ? (int32_t)plan->world - 1 : rank;
-  uint16_t gk[ORACLE_MAX_WORLD];
   for (int32_t r = r_first; r <= r_last; ++r) {
     int64_t lo = (int64_t)r * plan->shard;
     int64_t hi = lo + plan->shard;
@@ -219,12 +256,23 @@ int oracle_zero_step(const oracle_plan_t* plan, int32_t rank, int64_t i0, int64_
     if (lo < i0) lo = i0;
     if (hi > i1) hi = i1;
     for (int64_t i = lo; i < hi; ++i) {
-      for (int32_t k = 0; k < plan->world; ++k) gk[k] = grads[k][i - grad_base];
-      oracle_adam_element(gk, (int32_t)plan->world, &s, &master[i - state_base],
-                          &m[i - state_base], &v[i - state_base], &param[i - param_base]);
+      const float acc =
+          oracle_reduce(grads, grad_f32, acc_bf16, (int32_t)plan->world, i - grad_base);
+      oracle_adam_element(acc, &s, &master[i - state_base], &m[i - state_base],
+                          &v[i - state_base], &param[i - param_base]);
     }
   }
   return 0;
+}
+
+/* The method: bf16 gradients, fp32 rank-ordered sum. */
+int oracle_zero_step(const oracle_plan_t* plan, int32_t rank, int64_t i0, int64_t i1,
+                     const uint16_t* const* grads, int64_t grad_base, float* master, float* m,
+                     float* v, int64_t state_base, uint16_t* param, int64_t param_base, double lr,
+                     double beta1, double beta2, double eps, int64_t t) {
+  return oracle_zero_step_ex(plan, rank, i0, i1, (const void* const*)grads, grad_base, 0, 0,
+                             master, m, v, state_base, param, param_base, lr, beta1, beta2, eps,
+                             t);
 }
 
 /*

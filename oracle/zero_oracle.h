@@ -14,6 +14,7 @@ typedef struct {
   uint64_t bytes_dp, bytes_z1, bytes_z2, bytes_z3;
   double formula_dp, formula_z1, formula_z2, formula_z3;
   uint64_t state_bytes_rank;
+  double comm_dp, comm_z1, comm_z2, comm_z3;
 } oracle_plan_t;
 
 typedef struct {
@@ -29,6 +30,11 @@ int oracle_zero_step(const oracle_plan_t* plan, int32_t rank, int64_t i0, int64_
                      const uint16_t* const* grads, int64_t grad_base, float* master, float* m,
                      float* v, int64_t state_base, uint16_t* param, int64_t param_base, double lr,
                      double beta1, double beta2, double eps, int64_t t);
+int oracle_zero_step_ex(const oracle_plan_t* plan, int32_t rank, int64_t i0, int64_t i1,
+                        const void* const* grads, int64_t grad_base, int grad_f32, int acc_bf16,
+                        float* master, float* m, float* v, int64_t state_base, uint16_t* param,
+                        int64_t param_base, double lr, double beta1, double beta2, double eps,
+                        int64_t t);
 int oracle_dp_step(int64_t numel, int32_t world, const uint16_t* const* grads, float* master,
                    float* m, float* v, uint16_t* param, double lr, double beta1, double beta2,
                    double eps, int64_t t);

@@ -49,8 +49,10 @@ def test_plan_matches_oracle_brute_force(za):
             for k in ("numel", "world", "shard", "pad", "padded", "bytes_dp", "bytes_z1",
                       "bytes_z2", "bytes_z3", "state_bytes_rank"):
                 assert getattr(p, k) == o[k], (numel, world, k)
-            for k in ("formula_dp", "formula_z1", "formula_z2", "formula_z3"):
-                assert math.isclose(getattr(p, k), o[k], rel_tol=1e-15), (numel, world, k)
+            for k in ("formula_dp", "formula_z1", "formula_z2", "formula_z3", "comm_dp",
+                      "comm_z1", "comm_z2", "comm_z3"):
+                assert math.isclose(getattr(p, k), o[k], rel_tol=1e-14, abs_tol=1e-9), \
+                    (numel, world, k)
 
 
 def test_plan_config_sizes(za):
@@ -122,7 +124,7 @@ def test_step_argument_errors(za):
     assert _step(za, plan, b1=1.0) == codes["ZERO_E_HPARAM"]
     assert _step(za, plan, b2=-0.1) == codes["ZERO_E_HPARAM"]
     assert _step(za, plan, eps=float("inf")) == codes["ZERO_E_HPARAM"]
-    assert _step(za, plan, layout=2) == codes["ZERO_E_LAYOUT"]
+    assert _step(za, plan, layout=3) == codes["ZERO_E_LAYOUT"]
     assert _step(za, plan, layout=1) == codes["ZERO_E_LAYOUT"]      # shard grads, all ranks
     assert _step(za, plan, player=1) == codes["ZERO_E_LAYOUT"]      # shard params, all ranks
     assert _step(za, plan, master=0) == codes["ZERO_E_NULLPTR"]
@@ -141,6 +143,37 @@ def test_step_argument_errors(za):
     # single rank owning no real element: valid, nothing to do, no CUDA call
     empty = za.zero_plan(9, 4)   # shard 3: rank 3 owns [9, 12), all padding
     assert _step(za, empty, rank=3, layout=1, player=1) == 0
+
+
+def test_range_argument_errors(za):
+    plan = za.zero_plan(1000, 4)
+    lib = za.raw_lib()
+    codes = {v: k for k, v in za.ERRORS.items()}
+    g = [BASE + 5 * 2**30 + k * 2**28 for k in range(4)]
+    ptrs = (ctypes.c_void_p * 4)(*g)
+
+    def rng(begin, end, layout=2, rank=-1, player=0, master=BASE + 2**30):
+        return lib.zero_adam_step_range(ctypes.byref(plan), rank, begin, end, ptrs, layout,
+                                        master, BASE + 2 * 2**30, BASE + 3 * 2**30,
+                                        BASE + 4 * 2**30, player, 1e-3, .9, .999, 1e-8, 1, None)
+
+    assert rng(-1, 10) == codes["ZERO_E_RANGE"]
+    assert rng(20, 10) == codes["ZERO_E_RANGE"]
+    assert rng(0, 10, layout=3) == codes["ZERO_E_LAYOUT"]
+    assert rng(0, 10, layout=0x40) == codes["ZERO_E_LAYOUT"]            # unknown flag
+    assert rng(0, 10, master=BASE + 2**30 + 2) == codes["ZERO_E_ALIGN"]
+    # fp32 gradients must be 4-byte aligned
+    ptrs2 = (ctypes.c_void_p * 4)(*[x + 2 for x in g])
+    assert lib.zero_adam_step_range(ctypes.byref(plan), -1, 0, 10, ptrs2, 2 | 0x10,
+                                    BASE + 2**30, BASE + 2 * 2**30, BASE + 3 * 2**30,
+                                    BASE + 4 * 2**30, 0, 1e-3, .9, .999, 1e-8, 1,
+                                    None) == codes["ZERO_E_ALIGN"]
+    # windows that hold none of the stepped rank's elements: valid, nothing launched
+    assert rng(0, 0) == 0
+    assert rng(2000, 3000) == 0
+    assert rng(0, 100, rank=2) == 0        # rank 2 owns [500, 750)
+    # zero_adam_step itself has no window layout
+    assert _step(za, plan, layout=2) == codes["ZERO_E_LAYOUT"]
 
 
 def test_gather_argument_errors(za):

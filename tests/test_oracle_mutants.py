@@ -19,10 +19,19 @@ MUTANTS = {
     "eps_inside_sqrt": ("sqrtf(v_hat) + s->eps", "sqrtf(v_hat + s->eps)"),
     "no_average": ("const float g = acc / s->world;", "const float g = acc;"),
     "reverse_rank_order": (
-        "float acc = oracle_bf16_to_f32(gk[0]);\n"
-        "  for (int32_t k = 1; k < world; ++k) acc = acc + oracle_bf16_to_f32(gk[k]);",
-        "float acc = oracle_bf16_to_f32(gk[world - 1]);\n"
-        "  for (int32_t k = world - 2; k >= 0; --k) acc = acc + oracle_bf16_to_f32(gk[k]);"),
+        "float acc = oracle_grad(grads, grad_f32, 0, idx);\n"
+        "  if (acc_bf16) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(acc));\n"
+        "  for (int32_t k = 1; k < world; ++k) {",
+        "float acc = oracle_grad(grads, grad_f32, world - 1, idx);\n"
+        "  if (acc_bf16) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(acc));\n"
+        "  for (int32_t k = world - 2; k >= 0; --k) {"),
+    "bf16_sum_not_rounded": (
+        "    acc = acc + oracle_grad(grads, grad_f32, k, idx);\n"
+        "    if (acc_bf16) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(acc));",
+        "    acc = acc + oracle_grad(grads, grad_f32, k, idx);"),
+    "f32_grads_truncated": ("if (grad_f32) return ((const float*)grads[k])[idx];",
+                            "if (grad_f32) return oracle_bf16_to_f32("
+                            "(uint16_t)(*(const uint32_t*)&((const float*)grads[k])[idx] >> 16));"),
     "no_bias_correction_m": ("const float m_hat = mm / s->bc1;", "const float m_hat = mm;"),
     "bias_power_t_minus_1": ("pow(beta2, (double)t)", "pow(beta2, (double)(t - 1))"),
     "update_sign": ("ww = ww - upd;", "ww = ww + upd;"),
@@ -38,6 +47,10 @@ MUTANTS = {
     "gather_wrong_shard": ("if (idx < unit_numel) full[idx] = shards[r][j];",
                            "if (idx < unit_numel) full[idx] = shards[(r + 1) % world][j];"),
     "dp_step_no_average": ("avg[i] = acc / s.world;", "avg[i] = acc;"),
+    "zero3_one_gather": ("out->comm_z3 = all_gather + all_gather + reduce_scatter;",
+                         "out->comm_z3 = all_gather + reduce_scatter;"),
+    "ring_share_whole_vector": ("const double ring_share = ((double)world - 1.0) / (double)world;",
+                                "const double ring_share = 1.0;"),
 }
 
 

@@ -125,6 +125,25 @@ def test_plan_demo_mlp(golden_dir):
     assert round(full / p["state_bytes_rank"]) == g["printed_ratio"]
 
 
+def test_plan_communication_ledger(golden_dir):
+    g = _golden(golden_dir, "memory_ledger.json")["communication"]
+    for world in (1, 2, 3, 8, 16, 64):
+        for numel in (12, 1000, 10**9):
+            p = oracle.plan(numel, world)
+            grad_bytes = 2 * p["padded"]
+            assert p["comm_dp"] == pytest.approx(2 * (world - 1) / world * grad_bytes, rel=1e-15)
+            assert p["comm_z1"] / max(p["comm_dp"], 1e-300) == pytest.approx(g["zero12_vs_dp"]) \
+                or world == 1
+            assert p["comm_z2"] == p["comm_z1"]
+            if world > 1:
+                assert p["comm_z3"] / p["comm_dp"] == pytest.approx(g["zero3_vs_dp"], rel=1e-15)
+            else:
+                assert p["comm_dp"] == p["comm_z3"] == 0.0
+    big = oracle.plan(10**12, 10**6)
+    assert big["comm_dp"] / big["numel"] == pytest.approx(g["dp_large_n_bytes_per_param"],
+                                                          rel=1e-5)
+
+
 def test_plan_rejects_bad_arguments():
     for numel, world in ((0, 1), (-5, 2), (10, 0), (10, -1)):
         with pytest.raises(ValueError):
@@ -474,3 +493,67 @@ def test_synth_windows_are_consistent():
     s = synth.Spec(seed=9, stream=4, rank=2, step=3, dist=synth.STUDENT_T3, sigma=1e-3)
     whole = synth.fill_host(s, 0, 5000, synth.OUT_BF16)
     assert (synth.fill_host(s, 1234, 77, synth.OUT_BF16) == whole[1234:1311]).all()
+
+
+# ------------------------------------------------- gradient variants (not the method)
+
+
+def test_fp32_gradients_match_torch_adam_demo_setting():
+    """The page's runnable demo keeps fp32 gradients: 4 ranks, the demo MLP's
+    19,210 parameters, lr 1e-2, 3 steps, against torch.optim.Adam on the average;
+    the page's bar is max |diff| < 1e-5."""
+    numel, world, lr = 19210, 4, 1e-2
+    rng = np.random.default_rng(21)
+    p = oracle.plan(numel, world)
+    w0 = rng.normal(0, 0.05, numel).astype(np.float32)
+    W = np.zeros(p["padded"], np.float32)
+    W[:numel] = w0
+    M, V = np.zeros_like(W), np.zeros_like(W)
+    par = np.zeros(numel, np.uint16)
+    ref = torch.nn.Parameter(torch.from_numpy(w0.copy()))
+    opt = torch.optim.Adam([ref], lr=lr, betas=(B1, B2), eps=EPS, foreach=False, fused=False)
+    for t in range(1, 4):
+        rows = [rng.normal(0, 1e-2, numel).astype(np.float32) for _ in range(world)]
+        grads = [np.pad(r, (0, p["padded"] - numel)) for r in rows]
+        oracle.zero_step(numel, world, -1, grads, W, M, V, par, lr, B1, B2, EPS, t, grad_f32=True)
+        acc = rows[0].copy()
+        for r in rows[1:]:
+            acc = acc + r
+        ref.grad = torch.from_numpy(acc / np.float32(world))
+        opt.step()
+    st = opt.state[ref]
+    w_ref = ref.detach().numpy()
+    assert np.abs(W[:numel] - w_ref).max() < 1e-5
+    assert np.allclose(W[:numel], w_ref, rtol=1e-6, atol=2e-8)
+    m_ref = st["exp_avg"].numpy()
+    assert np.allclose(M[:numel], m_ref, rtol=1e-6, atol=1e-6 * np.abs(m_ref).max())
+
+
+def test_bf16_accumulation_rounds_each_partial_sum():
+    """In bf16 (8 significant bits) 1 + 2^-8 ties to 1, twice; the fp32 sum is 1 + 2^-7.
+    With beta1 = 0 the first moment is the averaged gradient itself."""
+    h = 2.0**-8
+    rows = [_bf16([1.0]), _bf16([h]), _bf16([h])]
+    numel, world = 1, 3
+    p = oracle.plan(numel, world)
+    grads = [np.pad(r, (0, p["padded"] - numel)) for r in rows]
+
+    def run(acc_bf16):
+        W = np.zeros(p["padded"], np.float32)
+        M, V = np.zeros_like(W), np.zeros_like(W)
+        oracle.zero_step(numel, world, -1, grads, W, M, V, np.zeros(1, np.uint16), LR, 0.0, 0.0,
+                         EPS, 1, acc_bf16=acc_bf16)
+        return M[0]
+
+    assert run(True) == np.float32(1.0) / np.float32(3.0)
+    assert run(False) == np.float32(1.0 + 2.0**-7) / np.float32(3.0)
+    # one rank: nothing is added, so the variant is the method (bf16 gradients)
+    rng = np.random.default_rng(22)
+    g = _bf16(rng.normal(0, 1e-3, 999))
+    outs = []
+    for acc in (False, True):
+        W = rng.normal(0, 0.02, 999).astype(np.float32) * 0 + 0.01
+        M, V, par = np.zeros(999, np.float32), np.zeros(999, np.float32), np.zeros(999, np.uint16)
+        oracle.zero_step(999, 1, -1, [g], W, M, V, par, LR, B1, B2, EPS, 1, acc_bf16=acc)
+        outs.append((W.copy(), M.copy()))
+    assert (outs[0][0].view(np.uint32) == outs[1][0].view(np.uint32)).all()

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libzeroadam.so")
 
 ZERO_OK = 0
 ZERO_ALL_RANKS = -1
-ZERO_GRAD_FULL, ZERO_GRAD_SHARD = 0, 1
+ZERO_GRAD_FULL, ZERO_GRAD_SHARD, ZERO_GRAD_WINDOW = 0, 1, 2
+ZERO_GRAD_F32, ZERO_ACC_BF16 = 0x10, 0x20
 ZERO_PARAM_FULL, ZERO_PARAM_SHARD = 0, 1
 ZERO_MAX_WORLD = 1024
 
@@ -27,10 +28,12 @@ ERRORS = {
     -1: "ZERO_E_NULLPTR", -2: "ZERO_E_WORLD", -3: "ZERO_E_NUMEL", -4: "ZERO_E_RANK",
     -5: "ZERO_E_STEP", -6: "ZERO_E_ALIGN", -7: "ZERO_E_HPARAM", -8: "ZERO_E_LAYOUT",
     -9: "ZERO_E_PLAN", -10: "ZERO_E_ALIAS", -11: "ZERO_E_LAUNCH", -12: "ZERO_E_DEVICE",
+    -13: "ZERO_E_RANGE",
 }
 
 # Every symbol include/zeroadam.h declares.
-EXPORTS = ("zero_plan", "zero_adam_step", "zero3_unit_gather", "zero_strerror", "zero_version")
+EXPORTS = ("zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
+           "zero_strerror", "zero_version")
 
 
 class ZeroError(RuntimeError):
@@ -71,6 +74,9 @@ def _load() -> ctypes.CDLL:
     lib.zero_adam_step.argtypes = [ctypes.POINTER(ZeroPlan), i32, vp, i32, vp, vp, vp, vp, i32,
                                    dbl, dbl, dbl, dbl, i64, vp]
     lib.zero_adam_step.restype = ctypes.c_int
+    lib.zero_adam_step_range.argtypes = [ctypes.POINTER(ZeroPlan), i32, i64, i64, vp, i32, vp, vp,
+                                         vp, vp, i32, dbl, dbl, dbl, dbl, i64, vp]
+    lib.zero_adam_step_range.restype = ctypes.c_int
     lib.zero3_unit_gather.argtypes = [ctypes.POINTER(ZeroPlan), vp, vp, vp]
     lib.zero3_unit_gather.restype = ctypes.c_int
     lib.zero_strerror.argtypes = [ctypes.c_int]
@@ -136,6 +142,25 @@ def zero_adam_step(plan: ZeroPlan, rank: int, grads, master, m, v, param, *, lr:
         raise ZeroError(rc, "zero_adam_step")
 
 
+def zero_adam_step_range(plan: ZeroPlan, rank: int, begin: int, end: int, grads, master, m, v,
+                         param, *, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                         eps: float = 1e-8, t: int, grad_layout: int = ZERO_GRAD_WINDOW,
+                         param_layout: int = ZERO_PARAM_FULL, stream=None) -> None:
+    """The step on the global flat window [begin, end) only (one ZeRO-2 bucket).
+
+    With ZERO_GRAD_WINDOW (the default here) each gradient buffer holds only the
+    window: element i at grads[k][i - begin].
+    """
+    ptrs = (ctypes.c_void_p * len(grads))(*[_addr(g) for g in grads])
+    if len(grads) != plan.world:
+        raise ValueError(f"expected {plan.world} gradient buffers, got {len(grads)}")
+    rc = _lib.zero_adam_step_range(ctypes.byref(plan), rank, begin, end, ptrs, grad_layout,
+                                   _addr(master), _addr(m), _addr(v), _addr(param), param_layout,
+                                   lr, beta1, beta2, eps, t, _stream_handle(stream))
+    if rc != ZERO_OK:
+        raise ZeroError(rc, "zero_adam_step_range")
+
+
 def zero3_unit_gather(unit_plan: ZeroPlan, shards, full, stream=None) -> None:
     """ZeRO-3 unit all-gather: the `world` bf16 shards -> the unit's full bf16 buffer."""
     if len(shards) != unit_plan.world:
@@ -156,6 +181,7 @@ def raw_lib() -> ctypes.CDLL:
     return _lib
 
 
-__all__ = ["zero_plan", "zero_adam_step", "zero3_unit_gather", "ZeroPlan", "ZeroError",
-           "strerror", "version", "raw_lib", "ZERO_ALL_RANKS", "ZERO_GRAD_FULL",
-           "ZERO_GRAD_SHARD", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "EXPORTS", "LIB_PATH"]
+__all__ = ["zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
+           "ZeroPlan", "ZeroError", "strerror", "version", "raw_lib", "ZERO_ALL_RANKS",
+           "ZERO_GRAD_FULL", "ZERO_GRAD_SHARD", "ZERO_GRAD_WINDOW", "ZERO_GRAD_F32",
+           "ZERO_ACC_BF16", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "EXPORTS", "LIB_PATH"]

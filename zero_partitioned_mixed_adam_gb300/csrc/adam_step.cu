@@ -2,16 +2,17 @@
 //
 // One pass over the stepped flat range does all of "ZeRO and FSDP" ->
 // "Implementing ZeRO's Adam from scratch", ZeroAdam.step:
-//   reduce-scatter + average  : sum of the N ranks' bf16 gradients, fp32, in
-//                               rank order 0..N-1, divided by N
+//   reduce-scatter + average  : sum of the N ranks' gradients, fp32, in rank
+//                               order 0..N-1, divided by N
 //   Adam + bias correction    : fp32 master, m, v updated in place
 //   all-gather + unflatten    : bf16 (round to nearest even) of the new master
 //                               stored straight into the flat parameter buffer
 // The reduced gradient never leaves registers.  Per element the kernel moves
-// 2N (gradients) + 12 (state read) + 12 (state write) + 2 (bf16 parameter)
-// bytes and does ~20 fp32 operations: it is bound by HBM bandwidth, so it is
-// written as a streaming kernel (16-byte vector loads/stores, a persistent
-// grid-stride loop sized to the SM count) and uses no tensor cores.
+// N*sizeof(grad) (gradients) + 12 (state read) + 12 (state write) + 2 (bf16
+// parameter) bytes and does ~20 fp32 operations: it is bound by HBM
+// bandwidth, so it is written as a streaming kernel (16-byte vector
+// loads/stores, a persistent grid-stride loop sized to the SM count) and uses
+// no tensor cores.
 //
 // Bit-exactness: every operation is an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nvcc cannot contract any
@@ -19,6 +20,11 @@
 // kept and division and square root are IEEE-correct.  The one rewrite is
 // g/N -> g*(1/N) when N is a power of two, which is the same correctly
 // rounded real number (1/N is exact).
+//
+// Variants (template parameters): gradients in bf16 (the mixed-precision
+// setting) or fp32 (the page's runnable demo keeps fp32 gradients); the sum
+// over ranks kept in fp32 (the method) or rounded to bf16 after every
+// addition (what a reduce-scatter on bf16 buffers delivers).
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -34,7 +40,7 @@ constexpr int kTableRuntime = 1024;  // gradient-pointer table of the any-N kern
 
 template <int CAP>
 struct StepArgs {
-  const uint16_t* g[CAP];  // rank k's gradient, at the range's first element
+  const void* g[CAP];  // rank k's gradient, at the range's first element
   float* master;
   float* m;
   float* v;
@@ -60,6 +66,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
          (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
 }
 
+// One step of the running sum over ranks.
+template <bool ABF16>
+__device__ __forceinline__ float acc_add(float acc, float x) {
+  const float s = __fadd_rn(acc, x);
+  if (ABF16) return bf16_to_f32(f32_to_bf16_rn(s));
+  return s;
+}
+
 // Adam with bias correction on one element, in ZeroAdam.step's order.
 __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, float& w, float& m,
                                              float& v) {
@@ -72,49 +86,77 @@ __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, f
   w = __fsub_rn(w, __fdiv_rn(__fmul_rn(s.lr, m_hat), denom));
 }
 
-// acc[j] += rank-k gradient of element e0+j, for a 16-byte vector of 8 bf16.
-__device__ __forceinline__ void accumulate8(float acc[8], const uint4 r) {
-  acc[0] = __fadd_rn(acc[0], bf16_lo(r.x));
-  acc[1] = __fadd_rn(acc[1], bf16_hi(r.x));
-  acc[2] = __fadd_rn(acc[2], bf16_lo(r.y));
-  acc[3] = __fadd_rn(acc[3], bf16_hi(r.y));
-  acc[4] = __fadd_rn(acc[4], bf16_lo(r.z));
-  acc[5] = __fadd_rn(acc[5], bf16_hi(r.z));
-  acc[6] = __fadd_rn(acc[6], bf16_lo(r.w));
-  acc[7] = __fadd_rn(acc[7], bf16_hi(r.w));
+// 8 gradients of one rank as fp32, loaded as 16-byte vectors.
+template <bool GF32>
+struct GradVec;
+
+template <>
+struct GradVec<false> {  // 8 bf16 = one 16-byte vector
+  uint4 r;
+  __device__ __forceinline__ void load(const void* p, int64_t e0) {
+    r = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + e0));
+  }
+  __device__ __forceinline__ float get(int j) const {
+    const uint32_t w = j < 2 ? r.x : j < 4 ? r.y : j < 6 ? r.z : r.w;
+    return (j & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
+};
+
+template <>
+struct GradVec<true> {  // 8 fp32 = two 16-byte vectors
+  float4 a, b;
+  __device__ __forceinline__ void load(const void* p, int64_t e0) {
+    const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(p) + e0);
+    a = __ldcs(q);
+    b = __ldcs(q + 1);
+  }
+  __device__ __forceinline__ float get(int j) const {
+    const float4& h = j < 4 ? a : b;
+    const int i = j & 3;
+    return i == 0 ? h.x : i == 1 ? h.y : i == 2 ? h.z : h.w;
+  }
+};
+
+template <bool GF32>
+__device__ __forceinline__ float grad_scalar(const void* p, int64_t e) {
+  if (GF32) return __ldcs(static_cast<const float*>(p) + e);
+  return bf16_to_f32(__ldcs(static_cast<const uint16_t*>(p) + e));
 }
 
 // Sum over ranks of 8 consecutive elements.  The accumulator starts at -0.0,
 // the exact identity of IEEE addition (-0 + x == x for every x, +0 included),
 // so the result equals g_0 + g_1 + ... + g_{N-1} evaluated from g_0.
-template <int NT, int CAP>
+template <int NT, int CAP, bool GF32, bool ABF16>
 __device__ __forceinline__ void sum_grads8(const StepArgs<CAP>& a, int world, int64_t e0,
                                            float acc[8]) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = -0.0f;
   if (a.gvec) {
     // Ranks in groups: all of a group's 16-byte loads are issued before any
-    // of them is consumed, so up to G*16 bytes per thread are in flight.
-    constexpr int G = (NT > 0 && NT <= 16) ? NT : 8;
+    // of them is consumed.
+    constexpr int GMAX = GF32 ? 8 : 16;
+    constexpr int G = (NT > 0 && NT <= GMAX) ? NT : 8;
 #pragma unroll 1
     for (int k0 = 0; k0 < world; k0 += G) {
-      uint4 r[G];
+      GradVec<GF32> r[G];
 #pragma unroll
       for (int j = 0; j < G; ++j)
-        if (NT > 0 || k0 + j < world)
-          r[j] = __ldcs(reinterpret_cast<const uint4*>(a.g[k0 + j] + e0));
+        if (NT > 0 || k0 + j < world) r[j].load(a.g[k0 + j], e0);
 #pragma unroll
       for (int j = 0; j < G; ++j)
-        if (NT > 0 || k0 + j < world) accumulate8(acc, r[j]);
+        if (NT > 0 || k0 + j < world) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = acc_add<ABF16>(acc[i], r[j].get(i));
+        }
     }
   } else {
 #pragma unroll 1
     for (int k = 0; k < world; ++k) {
-      uint16_t h[8];
+      float x[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) h[j] = __ldcs(a.g[k] + e0 + j);
+      for (int j = 0; j < 8; ++j) x[j] = grad_scalar<GF32>(a.g[k], e0 + j);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], bf16_to_f32(h[j]));
+      for (int j = 0; j < 8; ++j) acc[j] = acc_add<ABF16>(acc[j], x[j]);
     }
   }
 }
@@ -153,11 +195,11 @@ __device__ __forceinline__ void store_bf16x8_rn(uint16_t* p, bool vec, const flo
 }
 
 // One element, no vector access (range head and tail).
-template <int NT, int CAP>
+template <int NT, int CAP, bool GF32, bool ABF16>
 __device__ __forceinline__ void step_element(const StepArgs<CAP>& a, int world, int64_t e) {
   float acc = -0.0f;
 #pragma unroll 1
-  for (int k = 0; k < world; ++k) acc = __fadd_rn(acc, bf16_to_f32(__ldcs(a.g[k] + e)));
+  for (int k = 0; k < world; ++k) acc = acc_add<ABF16>(acc, grad_scalar<GF32>(a.g[k], e));
   float w = a.master[e], mm = a.m[e], vv = a.v[e];
   adam_element(acc, a.s, w, mm, vv);
   a.master[e] = w;
@@ -166,7 +208,7 @@ __device__ __forceinline__ void step_element(const StepArgs<CAP>& a, int world, 
   a.param[e] = f32_to_bf16_rn(w);
 }
 
-template <int NT, int CAP>
+template <int NT, int CAP, bool GF32, bool ABF16>
 __global__ void __launch_bounds__(kThreads)
     zero_adam_step_kernel(const __grid_constant__ StepArgs<CAP> a) {
   const int world = NT > 0 ? NT : a.world;
@@ -176,7 +218,7 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t q = tid; q < a.nvec; q += nthreads) {
     const int64_t e0 = a.head + 8 * q;
     float acc[8], w[8], mm[8], vv[8];
-    sum_grads8<NT, CAP>(a, world, e0, acc);
+    sum_grads8<NT, CAP, GF32, ABF16>(a, world, e0, acc);
     load_f32x8(a.master + e0, a.svec, w);
     load_f32x8(a.m + e0, a.svec, mm);
     load_f32x8(a.v + e0, a.svec, vv);
@@ -187,9 +229,9 @@ __global__ void __launch_bounds__(kThreads)
     store_f32x8(a.v + e0, a.svec, vv);
     store_bf16x8_rn(a.param + e0, a.pvec, w);
   }
-  for (int64_t e = tid; e < a.head; e += nthreads) step_element<NT, CAP>(a, world, e);
+  for (int64_t e = tid; e < a.head; e += nthreads) step_element<NT, CAP, GF32, ABF16>(a, world, e);
   for (int64_t e = a.head + 8 * a.nvec + tid; e < a.n; e += nthreads)
-    step_element<NT, CAP>(a, world, e);
+    step_element<NT, CAP, GF32, ABF16>(a, world, e);
 }
 
 // Resident blocks per SM of a kernel on the current device (cached).
@@ -214,7 +256,7 @@ inline int residue(const void* p, int esize) {
   return static_cast<int>((reinterpret_cast<uintptr_t>(p) / esize) % (16 / esize));
 }
 
-template <int NT, int CAP>
+template <int NT, int CAP, bool GF32, bool ABF16>
 cudaError_t launch_world(const StepLaunch& L) {
   StepArgs<CAP> a;
   for (int k = 0; k < L.world; ++k) a.g[k] = L.grads[k];
@@ -228,18 +270,20 @@ cudaError_t launch_world(const StepLaunch& L) {
   a.s = L.s;
 
   // Pick the body's start (head in 0..7) that lets the most bytes per element
-  // move as 16-byte vectors: all gradients together (2N B), the fp32 state
-  // (24 B), the bf16 parameters (2 B).  Buffers from cudaMalloc used whole
-  // are all aligned at head = 0.
-  int rg = residue(L.grads[0], 2);
+  // move as 16-byte vectors: all gradients together (N * 2 or 4 B), the fp32
+  // state (24 B), the bf16 parameters (2 B).  Buffers from cudaMalloc used
+  // whole are all aligned at head = 0.
+  const int gsize = GF32 ? 4 : 2;
+  const int gmod = 16 / gsize;
+  int rg = residue(L.grads[0], gsize);
   for (int k = 1; k < L.world; ++k)
-    if (residue(L.grads[k], 2) != rg) rg = -1;
+    if (residue(L.grads[k], gsize) != rg) rg = -1;
   int rs = residue(L.master, 4);
   if (residue(L.m, 4) != rs || residue(L.v, 4) != rs) rs = -1;
   const int rp = residue(L.param, 2);
   int best_h = 0, best_score = -1;
   for (int h = 0; h < 8; ++h) {
-    const int score = ((rg >= 0 && (rg + h) % 8 == 0) ? 2 * L.world : 0) +
+    const int score = ((rg >= 0 && (rg + h) % gmod == 0) ? gsize * L.world : 0) +
                       ((rs >= 0 && (rs + h) % 4 == 0) ? 24 : 0) + (((rp + h) % 8 == 0) ? 2 : 0);
     if (score > best_score) {
       best_score = score;
@@ -250,19 +294,34 @@ cudaError_t launch_world(const StepLaunch& L) {
   if (head > L.n) head = L.n;
   a.head = static_cast<int32_t>(head);
   a.nvec = (L.n - head) / 8;
-  a.gvec = (rg >= 0 && (rg + best_h) % 8 == 0);
+  a.gvec = (rg >= 0 && (rg + best_h) % gmod == 0);
   a.svec = (rs >= 0 && (rs + best_h) % 4 == 0);
   a.pvec = ((rp + best_h) % 8 == 0);
 
-  const void* kern = reinterpret_cast<const void*>(&zero_adam_step_kernel<NT, CAP>);
+  const void* kern = reinterpret_cast<const void*>(&zero_adam_step_kernel<NT, CAP, GF32, ABF16>);
   int sms = 0;
   if (device_sm_count(&sms) != 0) return cudaErrorNoDevice;
   const int64_t cap = static_cast<int64_t>(sms) * blocks_per_sm(kern);
   int64_t blocks = (a.nvec + kThreads - 1) / kThreads;
   if (blocks < 1) blocks = 1;
   if (blocks > cap) blocks = cap;
-  zero_adam_step_kernel<NT, CAP><<<static_cast<unsigned>(blocks), kThreads, 0, L.stream>>>(a);
+  zero_adam_step_kernel<NT, CAP, GF32, ABF16>
+      <<<static_cast<unsigned>(blocks), kThreads, 0, L.stream>>>(a);
   return cudaGetLastError();
+}
+
+template <bool GF32, bool ABF16>
+cudaError_t launch_variant(const StepLaunch& L) {
+  switch (L.world) {
+    case 1: return launch_world<1, 1, GF32, ABF16>(L);
+    case 2: return launch_world<2, 2, GF32, ABF16>(L);
+    case 4: return launch_world<4, 4, GF32, ABF16>(L);
+    case 8: return launch_world<8, 8, GF32, ABF16>(L);
+    case 16: return launch_world<16, 16, GF32, ABF16>(L);
+    case 32: return launch_world<32, 32, GF32, ABF16>(L);
+    case 64: return launch_world<64, 64, GF32, ABF16>(L);
+    default: return launch_world<0, kTableRuntime, GF32, ABF16>(L);
+  }
 }
 
 }  // namespace
@@ -270,16 +329,10 @@ cudaError_t launch_world(const StepLaunch& L) {
 cudaError_t launch_adam_step(const StepLaunch& L) {
   if (L.n <= 0) return cudaSuccess;
   (void)cudaGetLastError();  // launch errors below are this call's own
-  switch (L.world) {
-    case 1: return launch_world<1, 1>(L);
-    case 2: return launch_world<2, 2>(L);
-    case 4: return launch_world<4, 4>(L);
-    case 8: return launch_world<8, 8>(L);
-    case 16: return launch_world<16, 16>(L);
-    case 32: return launch_world<32, 32>(L);
-    case 64: return launch_world<64, 64>(L);
-    default: return launch_world<0, kTableRuntime>(L);
-  }
+  if (!L.grad_f32 && !L.acc_bf16) return launch_variant<false, false>(L);
+  if (!L.grad_f32 && L.acc_bf16) return launch_variant<false, true>(L);
+  if (L.grad_f32 && !L.acc_bf16) return launch_variant<true, false>(L);
+  return launch_variant<true, true>(L);
 }
 
 }  // namespace zeroadam

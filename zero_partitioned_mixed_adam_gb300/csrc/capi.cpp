@@ -120,20 +120,25 @@ int zero_plan(int64_t numel, int32_t world, zero_plan_t* out) {
   return make_plan(numel, world, out);
 }
 
-int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* grad_ptrs,
-                   int32_t grad_layout, float* master, float* m, float* v, void* param_bf16,
-                   int32_t param_layout, double lr, double beta1, double beta2, double eps,
-                   int64_t t, void* stream) {
+int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end,
+                         const void* const* grad_ptrs, int32_t grad_layout, float* master,
+                         float* m, float* v, void* param_bf16, int32_t param_layout, double lr,
+                         double beta1, double beta2, double eps, int64_t t, void* stream) {
   int rc = check_plan(plan);
   if (rc != ZERO_OK) return rc;
   const int32_t N = static_cast<int32_t>(plan->world);
   if (rank != ZERO_ALL_RANKS && (rank < 0 || rank >= N)) return ZERO_E_RANK;
-  if (grad_layout != ZERO_GRAD_FULL && grad_layout != ZERO_GRAD_SHARD) return ZERO_E_LAYOUT;
-  if (param_layout != ZERO_PARAM_FULL && param_layout != ZERO_PARAM_SHARD) return ZERO_E_LAYOUT;
-  if (rank == ZERO_ALL_RANKS && (grad_layout != ZERO_GRAD_FULL || param_layout != ZERO_PARAM_FULL))
+  const int32_t layout = grad_layout & ZERO_GRAD_LAYOUT_MASK;
+  const int32_t gflags = grad_layout & ~ZERO_GRAD_LAYOUT_MASK;
+  if (layout != ZERO_GRAD_FULL && layout != ZERO_GRAD_SHARD && layout != ZERO_GRAD_WINDOW)
     return ZERO_E_LAYOUT;
-  if (!is_finite(lr) || !is_finite(eps) || !is_finite(beta1) || !is_finite(beta2) || lr < 0.0 || eps < 0.0 ||
-      beta1 < 0.0 || beta1 >= 1.0 || beta2 < 0.0 || beta2 >= 1.0)
+  if ((gflags & ~(ZERO_GRAD_F32 | ZERO_ACC_BF16)) != 0) return ZERO_E_LAYOUT;
+  if (param_layout != ZERO_PARAM_FULL && param_layout != ZERO_PARAM_SHARD) return ZERO_E_LAYOUT;
+  if (rank == ZERO_ALL_RANKS && (layout == ZERO_GRAD_SHARD || param_layout != ZERO_PARAM_FULL))
+    return ZERO_E_LAYOUT;
+  if (begin < 0 || end < begin) return ZERO_E_RANGE;
+  if (!is_finite(lr) || !is_finite(eps) || !is_finite(beta1) || !is_finite(beta2) || lr < 0.0 ||
+      eps < 0.0 || beta1 < 0.0 || beta1 >= 1.0 || beta2 < 0.0 || beta2 >= 1.0)
     return ZERO_E_HPARAM;
   if (t < 1) return ZERO_E_STEP;
   if (grad_ptrs == nullptr || master == nullptr || m == nullptr || v == nullptr ||
@@ -142,26 +147,33 @@ int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* gra
   for (int32_t k = 0; k < N; ++k)
     if (grad_ptrs[k] == nullptr) return ZERO_E_NULLPTR;
 
-  // The stepped range of global flat indices, clipped to the real elements.
+  // The stepped range of global flat indices: the rank's (or every rank's)
+  // real elements, intersected with [begin, end).
   int64_t lo = 0, hi = plan->numel;
   if (rank != ZERO_ALL_RANKS) {
     lo = static_cast<int64_t>(rank) * plan->shard;
     hi = lo + plan->shard;
     if (hi > plan->numel) hi = plan->numel;
   }
-  const int64_t n = hi > lo ? hi - lo : 0;
-  // Where each buffer's element for global index lo sits.
-  const int64_t g_first = (grad_layout == ZERO_GRAD_FULL) ? lo : 0;
-  // master/m/v: all ranks' shards back to back (range starts at lo == 0), or
-  // one rank's shard (global index lo is its element 0).
-  const int64_t s_first = 0;
-  const int64_t p_first = (param_layout == ZERO_PARAM_FULL) ? lo : 0;
+  const int64_t a = begin > lo ? begin : lo;
+  const int64_t b = end < hi ? end : hi;
+  const int64_t n = b > a ? b - a : 0;
+  // Where each buffer holds global index a.
+  const int64_t g_first = layout == ZERO_GRAD_FULL ? a : layout == ZERO_GRAD_SHARD ? a - lo
+                                                                                   : a - begin;
+  // master/m/v: all ranks' shards back to back (global index), or one
+  // rank's shard (global index lo is its element 0).
+  const int64_t s_first = rank == ZERO_ALL_RANKS ? a : a - lo;
+  const int64_t p_first = param_layout == ZERO_PARAM_FULL ? a : a - lo;
+  const int gsize = (gflags & ZERO_GRAD_F32) ? 4 : 2;
 
-  auto odd2 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; };
-  auto odd4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
-  if (odd4(master) || odd4(m) || odd4(v) || odd2(param_bf16)) return ZERO_E_ALIGN;
+  auto misaligned = [](const void* p, uintptr_t k) {
+    return (reinterpret_cast<uintptr_t>(p) & (k - 1)) != 0;
+  };
+  if (misaligned(master, 4) || misaligned(m, 4) || misaligned(v, 4) || misaligned(param_bf16, 2))
+    return ZERO_E_ALIGN;
   for (int32_t k = 0; k < N; ++k)
-    if (odd2(grad_ptrs[k])) return ZERO_E_ALIGN;
+    if (misaligned(grad_ptrs[k], gsize)) return ZERO_E_ALIGN;
 
   if (n > 0) {
     const Range outs[4] = {bytes_of(master, s_first, n, 4), bytes_of(m, s_first, n, 4),
@@ -170,7 +182,7 @@ int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* gra
       for (int j = i + 1; j < 4; ++j)
         if (overlap(outs[i], outs[j])) return ZERO_E_ALIAS;
     for (int32_t k = 0; k < N; ++k) {
-      const Range g = bytes_of(grad_ptrs[k], g_first, n, 2);
+      const Range g = bytes_of(grad_ptrs[k], g_first, n, gsize);
       for (int i = 0; i < 4; ++i)
         if (overlap(g, outs[i])) return ZERO_E_ALIAS;
     }
@@ -178,12 +190,15 @@ int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* gra
   if (n == 0) return ZERO_OK;
 
   // Offset every pointer to the range's first element.
-  const uint16_t* g[ZERO_MAX_WORLD];
-  for (int32_t k = 0; k < N; ++k) g[k] = static_cast<const uint16_t*>(grad_ptrs[k]) + g_first;
+  const void* g[ZERO_MAX_WORLD];
+  for (int32_t k = 0; k < N; ++k)
+    g[k] = static_cast<const char*>(grad_ptrs[k]) + g_first * gsize;
 
   StepLaunch L;
   L.grads = g;
   L.world = N;
+  L.grad_f32 = (gflags & ZERO_GRAD_F32) ? 1 : 0;
+  L.acc_bf16 = (gflags & ZERO_ACC_BF16) ? 1 : 0;
   L.master = master + s_first;
   L.m = m + s_first;
   L.v = v + s_first;
@@ -203,6 +218,15 @@ int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* gra
   s.pow2_world = (N & (N - 1)) == 0 ? 1 : 0;
   s.inv_world = static_cast<float>(1.0 / static_cast<double>(N));
   return launch_status(launch_adam_step(L));
+}
+
+int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* grad_ptrs,
+                   int32_t grad_layout, float* master, float* m, float* v, void* param_bf16,
+                   int32_t param_layout, double lr, double beta1, double beta2, double eps,
+                   int64_t t, void* stream) {
+  if ((grad_layout & ZERO_GRAD_LAYOUT_MASK) == ZERO_GRAD_WINDOW) return ZERO_E_LAYOUT;
+  return zero_adam_step_range(plan, rank, 0, INT64_MAX, grad_ptrs, grad_layout, master, m, v,
+                              param_bf16, param_layout, lr, beta1, beta2, eps, t, stream);
 }
 
 int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs,
@@ -246,6 +270,7 @@ const char* zero_strerror(int status) {
     case ZERO_E_PLAN: return "plan fields differ from zero_plan(numel, world)";
     case ZERO_E_ALIAS: return "an output buffer overlaps another buffer";
     case ZERO_E_DEVICE: return "no usable CUDA device";
+    case ZERO_E_RANGE: return "the window must satisfy 0 <= begin <= end";
     case ZERO_E_LAUNCH:
       t_msg = std::string("kernel launch failed: ") + cudaGetErrorString(t_last_cuda);
       return t_msg.c_str();

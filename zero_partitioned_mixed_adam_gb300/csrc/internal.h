@@ -24,8 +24,10 @@ struct AdamScalars {
 // One launch of the fused step over a contiguous range of n flat elements.
 // Every pointer already points at the range's first element.
 struct StepLaunch {
-  const uint16_t* const* grads;  // host array of `world` device pointers (bf16)
+  const void* const* grads;  // host array of `world` device pointers (bf16, or fp32 if grad_f32)
   int32_t world;
+  int32_t grad_f32;  // gradients are fp32 (else bf16)
+  int32_t acc_bf16;  // the running sum over ranks is rounded to bf16 after every addition
   float* master;
   float* m;
   float* v;
