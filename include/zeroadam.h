@@ -56,6 +56,10 @@ extern "C" {
 #define ZERO_E_LAUNCH (-11) /* the CUDA launch failed; see zero_strerror            */
 #define ZERO_E_DEVICE (-12) /* no usable CUDA device                                */
 #define ZERO_E_RANGE (-13)  /* zero_adam_step_range: begin < 0 or end < begin       */
+#define ZERO_E_SHAPE (-14)  /* zero3_unit_gather_rows: bad tensor count or shape    */
+
+/* Largest tensor count of one zero3_unit_gather_rows unit. */
+#define ZERO_MAX_UNIT_TENSORS 256
 
 /* Largest world (number of emulated data-parallel ranks) accepted. */
 #define ZERO_MAX_WORLD 1024
@@ -195,6 +199,29 @@ int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, i
  */
 int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs,
                       void* full_bf16, void* stream);
+
+/*
+ * FSDP2-style unit gather ("ZeRO-3 and FSDP": FSDP2 represents every parameter
+ * as a DTensor sharded along dimension 0, so each rank holds a block of rows of
+ * each tensor).  The unit is ntensors row-major bf16 tensors, tensor i of
+ * rows[i] x cols[i] elements.  With R_i = ceil(rows[i] / world), rank r holds
+ * rows [r*R_i, min((r+1)*R_i, rows[i])) of tensor i, stored as R_i x cols[i]
+ * elements (rows past the tensor's end are padding and are not copied); its
+ * shard buffer is those blocks for i = 0..ntensors-1 back to back
+ * (sum_i R_i*cols[i] elements).  The gathered unit full_bf16 is the tensors
+ * back to back (sum_i rows[i]*cols[i] elements).  Bit-exact copy.  For one
+ * tensor whose rows divide by world this is zero3_unit_gather's layout.
+ *
+ *   rows, cols  host arrays of ntensors positive sizes, read before return.
+ *   shard_ptrs  host array of world device pointers (bf16 shards).
+ * Errors: ZERO_E_SHAPE (ntensors not in [1, ZERO_MAX_UNIT_TENSORS], a size < 1,
+ * or the unit's element count overflows), ZERO_E_WORLD, ZERO_E_NULLPTR,
+ * ZERO_E_ALIGN (odd pointer), ZERO_E_ALIAS (output overlaps a shard),
+ * ZERO_E_LAUNCH.
+ */
+int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t* cols,
+                           int32_t world, const void* const* shard_ptrs, void* full_bf16,
+                           void* stream);
 
 /* ------------------------------------------------------------------ misc */
 

@@ -97,6 +97,9 @@ def _L():
         lib.oracle_unit_gather.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                                            ctypes.c_void_p]
         lib.oracle_unit_gather.restype = ctypes.c_int
+        lib.oracle_unit_gather_rows.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_unit_gather_rows.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -191,4 +194,25 @@ def unit_gather(unit_numel: int, world: int, shards) -> np.ndarray:
     rc = _L().oracle_unit_gather(unit_numel, world, _ptr_array(shards), _ptr(full))
     if rc != 0:
         raise ValueError("oracle_unit_gather failed")
+    return full
+
+
+def rows_layout(shapes, world):
+    """Sizes of the FSDP2-style row-sharded layout: (shard elements per rank, unit elements)."""
+    shard = sum(-(-r // world) * c for r, c in shapes)
+    return shard, sum(r * c for r, c in shapes)
+
+
+def unit_gather_rows(shapes, world: int, shards) -> np.ndarray:
+    """FSDP2-style unit gather: tensors (rows, cols) sharded by rows -> the full unit."""
+    rows = np.array([r for r, _ in shapes], np.int64)
+    cols = np.array([c for _, c in shapes], np.int64)
+    shard_len, total = rows_layout(shapes, world)
+    for s in shards:
+        assert s.size == shard_len
+    full = np.zeros(total, dtype=np.uint16)
+    rc = _L().oracle_unit_gather_rows(len(shapes), _ptr(rows), _ptr(cols), world,
+                                      _ptr_array(shards), _ptr(full))
+    if rc != 0:
+        raise ValueError("oracle_unit_gather_rows failed")
     return full

@@ -336,3 +336,35 @@ int oracle_unit_gather(int64_t unit_numel, int32_t world, const uint16_t* const*
 void oracle_f32_to_bf16_array(const float* x, uint16_t* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(x[i]);
 }
+
+/*
+ * FSDP2-style unit gather ("ZeRO-3 and FSDP": FSDP2 keeps every parameter as a
+ * DTensor sharded along dimension 0; each rank holds a block of rows).  The
+ * unit is ntensors row-major tensors, tensor i of rows[i] x cols[i].  With
+ * R = ceil(rows[i] / world) rows per rank, rank r holds rows
+ * [r*R, min((r+1)*R, rows[i])) of tensor i, stored as R x cols[i] elements
+ * (rows past the tensor's end are padding); its shard is those blocks for
+ * i = 0, 1, ... back to back.  The gathered unit is the tensors back to back.
+ * Element (i, row, col) of the unit comes from rank row / R, local row
+ * row - rank*R.
+ */
+int oracle_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t* cols,
+                            int32_t world, const uint16_t* const* shards, uint16_t* full) {
+  if (ntensors < 1 || world < 1 || rows == NULL || cols == NULL || shards == NULL || full == NULL)
+    return -1;
+  int64_t full_off = 0, shard_off = 0;
+  for (int32_t i = 0; i < ntensors; ++i) {
+    if (rows[i] < 1 || cols[i] < 1) return -1;
+    int64_t R = rows[i] / world;
+    if (R * world < rows[i]) R += 1;
+    for (int64_t row = 0; row < rows[i]; ++row) {
+      const int64_t r = row / R;
+      const int64_t local = row - r * R;
+      for (int64_t col = 0; col < cols[i]; ++col)
+        full[full_off + row * cols[i] + col] = shards[r][shard_off + local * cols[i] + col];
+    }
+    full_off += rows[i] * cols[i];
+    shard_off += R * cols[i];
+  }
+  return 0;
+}

@@ -40,6 +40,8 @@ int oracle_dp_step(int64_t numel, int32_t world, const uint16_t* const* grads, f
                    double eps, int64_t t);
 int oracle_unit_gather(int64_t unit_numel, int32_t world, const uint16_t* const* shards,
                        uint16_t* full);
+int oracle_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t* cols,
+                            int32_t world, const uint16_t* const* shards, uint16_t* full);
 void oracle_f32_to_bf16_array(const float* x, uint16_t* out, int64_t n);
 
 #endif

@@ -191,6 +191,32 @@ def test_gather_argument_errors(za):
                                  None) == codes["ZERO_E_ALIAS"]
 
 
+def test_gather_rows_argument_errors(za):
+    lib = za.raw_lib()
+    codes = {v: k for k, v in za.ERRORS.items()}
+    shards = [BASE + k * 2**20 for k in range(4)]
+    ptrs = (ctypes.c_void_p * 4)(*shards)
+
+    def call(rows, cols, world=4, full=BASE + 2**30, p=ptrs, n=None):
+        n = len(rows) if n is None else n
+        r = (ctypes.c_int64 * max(1, len(rows)))(*rows)
+        c = (ctypes.c_int64 * max(1, len(cols)))(*cols)
+        return lib.zero3_unit_gather_rows(n, r, c, world, p, full, None)
+
+    assert call([10], [3], n=0) == codes["ZERO_E_SHAPE"]
+    assert call([10] * 257, [3] * 257) == codes["ZERO_E_SHAPE"]
+    assert call([10, 0], [3, 3]) == codes["ZERO_E_SHAPE"]
+    assert call([10, 5], [3, -1]) == codes["ZERO_E_SHAPE"]
+    assert call([2**40], [2**40]) == codes["ZERO_E_SHAPE"]
+    assert call([10], [3], world=0) == codes["ZERO_E_WORLD"]
+    assert call([10], [3], full=0) == codes["ZERO_E_NULLPTR"]
+    assert call([10], [3], full=BASE + 2**30 + 1) == codes["ZERO_E_ALIGN"]
+    assert call([10], [3], full=shards[2] + 4) == codes["ZERO_E_ALIAS"]
+    bad = (ctypes.c_void_p * 4)(shards[0], None, shards[2], shards[3])
+    assert call([10], [3], p=bad) == codes["ZERO_E_NULLPTR"]
+    assert za.rows_layout([(10, 3), (7, 2)], 4) == (3 * 3 + 2 * 2, 44)
+
+
 def test_strerror(za):
     for code in za.ERRORS:
         s = za.strerror(code)

@@ -129,3 +129,75 @@ def test_unit_sweep_gather_and_step(U, N):
         gu.assert_bf16_close(gu.to_host_u16(p[a:b]), hp, f"unit {U}/{N} param [{a},{b})")
     del g, w, m, v, p
     torch.cuda.empty_cache()
+
+
+def _rows_problem(shapes, world, seed, off=0):
+    shard_len, total = za.rows_layout(shapes, world)
+    host = [synth.fill_host(synth.Spec(seed=seed, stream=7, rank=r, sigma=0.02), 0, shard_len,
+                            synth.OUT_BF16) for r in range(world)]
+    dev = []
+    for r in range(world):
+        b = torch.full((shard_len + off + GUARD,), CANARY16, dtype=torch.int16, device="cuda")
+        v = b[off:off + shard_len]
+        v.copy_(torch.from_numpy(host[r].view(np.int16)))
+        dev.append(v)
+    return host, dev, total
+
+
+LLAMA_LAYER = [(4096, 4096)] * 4 + [(11008, 4096), (11008, 4096), (4096, 11008), (4096, 1),
+                                     (4096, 1)]
+
+
+@pytest.mark.parametrize("shapes,world", [
+    ([(10, 3)], 4), ([(7, 5), (1, 9), (13, 1)], 3), ([(3, 2)], 8), ([(64, 10)], 8),
+    ([(1000, 17), (999, 33), (5, 1)], 16), ([(300, 7)] * 20, 64), ([(257, 129)], 65),
+    ([(4096, 256), (11008, 256), (256, 1)], 8),
+])
+def test_gather_rows_vs_oracle(shapes, world):
+    host, dev, total = _rows_problem(shapes, world, seed=len(shapes) * 100 + world)
+    fb = torch.full((total + 2 * GUARD,), CANARY16, dtype=torch.int16, device="cuda")
+    full = fb[GUARD:GUARD + total]
+    za.zero3_unit_gather_rows(shapes, world, dev, full)
+    torch.cuda.synchronize()
+    ref = oracle.unit_gather_rows(shapes, world, host)
+    assert (gu.to_host_u16(full) == ref).all()
+    assert bool((fb[:GUARD] == CANARY16).all()) and bool((fb[GUARD + total:] == CANARY16).all())
+
+
+@pytest.mark.parametrize("off", [1, 3])
+def test_gather_rows_misaligned(off):
+    shapes, world = [(1001, 7), (33, 3)], 4
+    host, dev, total = _rows_problem(shapes, world, seed=5, off=off)
+    full = torch.empty(total + 1, dtype=torch.int16, device="cuda")[1:]
+    za.zero3_unit_gather_rows(shapes, world, dev, full)
+    torch.cuda.synchronize()
+    assert (gu.to_host_u16(full) == oracle.unit_gather_rows(shapes, world, host)).all()
+
+
+@pytest.mark.parametrize("world", [2, 8, 64])
+def test_gather_rows_llama_layer(world):
+    """One Llama-7B layer (4 attention 4096x4096, 3 MLP 11008x4096 / 4096x11008, 2 norms)
+    sharded by rows: the whole unit is compared with an independent device
+    reconstruction (torch concatenation of the row blocks) and, for N <= 8, with the
+    oracle on the host."""
+    shard_len, total = za.rows_layout(LLAMA_LAYER, world)
+    assert total == 202_383_360
+    shards = [torch.empty(shard_len, dtype=torch.int16, device="cuda") for _ in range(world)]
+    for r in range(world):
+        gu.dev_fill_into(shards[r], synth.Spec(seed=world, stream=7, rank=r, sigma=0.02), 0,
+                         synth.OUT_BF16)
+    full = torch.empty(total, dtype=torch.int16, device="cuda")
+    za.zero3_unit_gather_rows(LLAMA_LAYER, world, shards, full)
+    parts, off = [], 0
+    for rows, cols in LLAMA_LAYER:
+        R = -(-rows // world)
+        chunks = [s[off:off + R * cols].view(R, cols) for s in shards]
+        parts.append(torch.cat(chunks)[:rows].reshape(-1))
+        off += R * cols
+    assert torch.equal(full, torch.cat(parts))
+    torch.cuda.synchronize()
+    if world <= 8:
+        host = [gu.to_host_u16(s) for s in shards]
+        assert (gu.to_host_u16(full) == oracle.unit_gather_rows(LLAMA_LAYER, world, host)).all()
+    del shards, full, parts
+    torch.cuda.empty_cache()

@@ -47,6 +47,10 @@ MUTANTS = {
     "gather_wrong_shard": ("if (idx < unit_numel) full[idx] = shards[r][j];",
                            "if (idx < unit_numel) full[idx] = shards[(r + 1) % world][j];"),
     "dp_step_no_average": ("avg[i] = acc / s.world;", "avg[i] = acc;"),
+    "rows_shard_offset_unpadded": ("    shard_off += R * cols[i];",
+                                   "    shard_off += (rows[i] / world) * cols[i];"),
+    "rows_local_row_from_next_rank": ("      const int64_t local = row - r * R;",
+                                      "      const int64_t local = row - r * R + (r > 0 ? 1 : 0);"),
     "zero3_one_gather": ("out->comm_z3 = all_gather + all_gather + reduce_scatter;",
                          "out->comm_z3 = all_gather + reduce_scatter;"),
     "ring_share_whole_vector": ("const double ring_share = ((double)world - 1.0) / (double)world;",

@@ -557,3 +557,37 @@ def test_bf16_accumulation_rounds_each_partial_sum():
         oracle.zero_step(999, 1, -1, [g], W, M, V, par, LR, B1, B2, EPS, 1, acc_bf16=acc)
         outs.append((W.copy(), M.copy()))
     assert (outs[0][0].view(np.uint32) == outs[1][0].view(np.uint32)).all()
+
+
+def test_unit_gather_rows_brute_force():
+    """FSDP2-style dim-0 sharding: numpy builds each rank's row blocks (ceil-sized
+    chunks, zero rows past the end) and the gather must restore the tensors."""
+    rng = np.random.default_rng(23)
+    for _ in range(200):
+        world = int(rng.integers(1, 9))
+        shapes = [(int(rng.integers(1, 20)), int(rng.integers(1, 7)))
+                  for _ in range(int(rng.integers(1, 5)))]
+        tensors = [rng.integers(0, 2**16, r * c, dtype=np.uint64).astype(np.uint16).reshape(r, c)
+                   for r, c in shapes]
+        shards = []
+        for k in range(world):
+            parts = []
+            for t in tensors:
+                R = -(-t.shape[0] // world)
+                block = np.zeros((R, t.shape[1]), np.uint16)
+                rows = t[k * R:(k + 1) * R]
+                block[:rows.shape[0]] = rows
+                parts.append(block.ravel())
+            shards.append(np.concatenate(parts))
+        full = oracle.unit_gather_rows(shapes, world, shards)
+        assert (full == np.concatenate([t.ravel() for t in tensors])).all(), (world, shapes)
+
+
+def test_unit_gather_rows_one_tensor_with_divisible_rows_is_the_flat_gather():
+    """One tensor whose rows divide by N: the row blocks are the flat shards."""
+    rng = np.random.default_rng(24)
+    rows, cols, world = 64, 10, 8
+    shards = [rng.integers(0, 2**16, rows // world * cols, dtype=np.uint64).astype(np.uint16)
+              for _ in range(world)]
+    assert (oracle.unit_gather_rows([(rows, cols)], world, shards)
+            == oracle.unit_gather(rows * cols, world, shards)).all()

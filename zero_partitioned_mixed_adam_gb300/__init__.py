@@ -28,12 +28,12 @@ ERRORS = {
     -1: "ZERO_E_NULLPTR", -2: "ZERO_E_WORLD", -3: "ZERO_E_NUMEL", -4: "ZERO_E_RANK",
     -5: "ZERO_E_STEP", -6: "ZERO_E_ALIGN", -7: "ZERO_E_HPARAM", -8: "ZERO_E_LAYOUT",
     -9: "ZERO_E_PLAN", -10: "ZERO_E_ALIAS", -11: "ZERO_E_LAUNCH", -12: "ZERO_E_DEVICE",
-    -13: "ZERO_E_RANGE",
+    -13: "ZERO_E_RANGE", -14: "ZERO_E_SHAPE",
 }
 
 # Every symbol include/zeroadam.h declares.
 EXPORTS = ("zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero_strerror", "zero_version")
+           "zero3_unit_gather_rows", "zero_strerror", "zero_version")
 
 
 class ZeroError(RuntimeError):
@@ -79,6 +79,8 @@ def _load() -> ctypes.CDLL:
     lib.zero_adam_step_range.restype = ctypes.c_int
     lib.zero3_unit_gather.argtypes = [ctypes.POINTER(ZeroPlan), vp, vp, vp]
     lib.zero3_unit_gather.restype = ctypes.c_int
+    lib.zero3_unit_gather_rows.argtypes = [i32, vp, vp, i32, vp, vp, vp]
+    lib.zero3_unit_gather_rows.restype = ctypes.c_int
     lib.zero_strerror.argtypes = [ctypes.c_int]
     lib.zero_strerror.restype = ctypes.c_char_p
     lib.zero_version.argtypes = []
@@ -172,6 +174,27 @@ def zero3_unit_gather(unit_plan: ZeroPlan, shards, full, stream=None) -> None:
         raise ZeroError(rc, "zero3_unit_gather")
 
 
+def rows_layout(shapes, world: int):
+    """(elements of one rank's shard, elements of the unit) of the FSDP2-style layout."""
+    return (sum(-(-r // world) * c for r, c in shapes), sum(r * c for r, c in shapes))
+
+
+def zero3_unit_gather_rows(shapes, world: int, shards, full, stream=None) -> None:
+    """FSDP2-style gather: tensors of shapes [(rows, cols), ...] sharded by rows across
+    `world` ranks (rank r holds rows [r*R, (r+1)*R), R = ceil(rows/world), of each
+    tensor, back to back) -> the unit's tensors back to back."""
+    if len(shards) != world:
+        raise ValueError(f"expected {world} shards, got {len(shards)}")
+    n = len(shapes)
+    rows = (ctypes.c_int64 * max(n, 1))(*[int(r) for r, _ in shapes])
+    cols = (ctypes.c_int64 * max(n, 1))(*[int(c) for _, c in shapes])
+    ptrs = (ctypes.c_void_p * len(shards))(*[_addr(s) for s in shards])
+    rc = _lib.zero3_unit_gather_rows(n, rows, cols, world, ptrs, _addr(full),
+                                     _stream_handle(stream))
+    if rc != ZERO_OK:
+        raise ZeroError(rc, "zero3_unit_gather_rows")
+
+
 def version() -> int:
     return _lib.zero_version()
 
@@ -182,6 +205,7 @@ def raw_lib() -> ctypes.CDLL:
 
 
 __all__ = ["zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
+           "zero3_unit_gather_rows", "rows_layout",
            "ZeroPlan", "ZeroError", "strerror", "version", "raw_lib", "ZERO_ALL_RANKS",
            "ZERO_GRAD_FULL", "ZERO_GRAD_SHARD", "ZERO_GRAD_WINDOW", "ZERO_GRAD_F32",
            "ZERO_ACC_BF16", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "EXPORTS", "LIB_PATH"]

@@ -8,7 +8,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/zeroadam.h"
+#include "zeroadam.h"
 #include "internal.h"
 
 namespace zeroadam {
@@ -256,6 +256,49 @@ int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptr
   return launch_status(launch_unit_gather(L));
 }
 
+int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t* cols,
+                           int32_t world, const void* const* shard_ptrs, void* full_bf16,
+                           void* stream) {
+  if (ntensors < 1 || ntensors > ZERO_MAX_UNIT_TENSORS) return ZERO_E_SHAPE;
+  if (world < 1 || world > ZERO_MAX_WORLD) return ZERO_E_WORLD;
+  if (rows == nullptr || cols == nullptr || shard_ptrs == nullptr || full_bf16 == nullptr)
+    return ZERO_E_NULLPTR;
+  int64_t per_rank[ZERO_MAX_UNIT_TENSORS], full_off[ZERO_MAX_UNIT_TENSORS],
+      shard_off[ZERO_MAX_UNIT_TENSORS];
+  int64_t total = 0, shard_len = 0;
+  const int64_t lim = INT64_MAX / 4;
+  for (int32_t i = 0; i < ntensors; ++i) {
+    if (rows[i] < 1 || cols[i] < 1) return ZERO_E_SHAPE;
+    if (rows[i] > lim / cols[i]) return ZERO_E_SHAPE;
+    per_rank[i] = rows[i] / world + (rows[i] % world != 0 ? 1 : 0);
+    full_off[i] = total;
+    shard_off[i] = shard_len;
+    total += rows[i] * cols[i];
+    shard_len += per_rank[i] * cols[i];
+    if (total > lim || shard_len > lim) return ZERO_E_SHAPE;
+  }
+  for (int32_t k = 0; k < world; ++k)
+    if (shard_ptrs[k] == nullptr) return ZERO_E_NULLPTR;
+  if (reinterpret_cast<uintptr_t>(full_bf16) & 1u) return ZERO_E_ALIGN;
+  for (int32_t k = 0; k < world; ++k)
+    if (reinterpret_cast<uintptr_t>(shard_ptrs[k]) & 1u) return ZERO_E_ALIGN;
+  const Range out = bytes_of(full_bf16, 0, total, 2);
+  for (int32_t k = 0; k < world; ++k)
+    if (overlap(out, bytes_of(shard_ptrs[k], 0, shard_len, 2))) return ZERO_E_ALIAS;
+  GatherRowsLaunch L;
+  L.shards = reinterpret_cast<const uint16_t* const*>(shard_ptrs);
+  L.world = world;
+  L.ntensors = ntensors;
+  L.rows = rows;
+  L.cols = cols;
+  L.rows_per_rank = per_rank;
+  L.full_off = full_off;
+  L.shard_off = shard_off;
+  L.full = static_cast<uint16_t*>(full_bf16);
+  L.stream = static_cast<cudaStream_t>(stream);
+  return launch_status(launch_unit_gather_rows(L));
+}
+
 const char* zero_strerror(int status) {
   switch (status) {
     case ZERO_OK: return "ok";
@@ -271,6 +314,7 @@ const char* zero_strerror(int status) {
     case ZERO_E_ALIAS: return "an output buffer overlaps another buffer";
     case ZERO_E_DEVICE: return "no usable CUDA device";
     case ZERO_E_RANGE: return "the window must satisfy 0 <= begin <= end";
+    case ZERO_E_SHAPE: return "ntensors in [1, ZERO_MAX_UNIT_TENSORS] and sizes >= 1 required";
     case ZERO_E_LAUNCH:
       t_msg = std::string("kernel launch failed: ") + cudaGetErrorString(t_last_cuda);
       return t_msg.c_str();

@@ -47,10 +47,26 @@ struct GatherLaunch {
   cudaStream_t stream;
 };
 
+// One launch of the FSDP2-style (dim-0 row-sharded) unit gather.  Offsets are
+// in elements; rows_per_rank = ceil(rows / world).
+struct GatherRowsLaunch {
+  const uint16_t* const* shards;
+  int32_t world;
+  int32_t ntensors;
+  const int64_t* rows;
+  const int64_t* cols;
+  const int64_t* rows_per_rank;
+  const int64_t* full_off;
+  const int64_t* shard_off;
+  uint16_t* full;
+  cudaStream_t stream;
+};
+
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count(int* sms);
 
 cudaError_t launch_adam_step(const StepLaunch& L);
 cudaError_t launch_unit_gather(const GatherLaunch& L);
+cudaError_t launch_unit_gather_rows(const GatherRowsLaunch& L);
 
 }  // namespace zeroadam

@@ -104,7 +104,104 @@ cudaError_t launch_cap(const GatherLaunch& L) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// FSDP2-style unit gather: every (tensor i, rank r) block of rows is one
+// contiguous run in rank r's shard and one contiguous run of the unit, so the
+// gather is ntensors*world block copies.  blockIdx.y strides over the blocks,
+// blockIdx.x over a block's elements.
+
+constexpr int kMaxTensors = 256;
+
+template <int CAP>
+struct GatherRowsArgs {
+  const uint16_t* src[CAP];
+  uint16_t* full;
+  int32_t world, ntensors;
+  int64_t rows[kMaxTensors], cols[kMaxTensors], per_rank[kMaxTensors];
+  int64_t full_off[kMaxTensors], shard_off[kMaxTensors];
+};
+
+template <int CAP>
+__global__ void __launch_bounds__(kThreads)
+    zero3_unit_gather_rows_kernel(const __grid_constant__ GatherRowsArgs<CAP> a) {
+  const int64_t nseg = static_cast<int64_t>(a.ntensors) * a.world;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t seg = blockIdx.y; seg < nseg; seg += gridDim.y) {
+    const int i = static_cast<int>(seg / a.world);
+    const int r = static_cast<int>(seg - static_cast<int64_t>(i) * a.world);
+    const int64_t r0 = static_cast<int64_t>(r) * a.per_rank[i];
+    if (r0 >= a.rows[i]) continue;
+    int64_t nrows = a.rows[i] - r0;
+    if (nrows > a.per_rank[i]) nrows = a.per_rank[i];
+    const int64_t len = nrows * a.cols[i];
+    const uint16_t* __restrict__ src = a.src[r] + a.shard_off[i];
+    uint16_t* __restrict__ dst = a.full + a.full_off[i] + r0 * a.cols[i];
+    int64_t done = 0;
+    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0) {
+      const int64_t nv = len / 8;
+      const uint4* s4 = reinterpret_cast<const uint4*>(src);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      int64_t q = tid;
+      for (; q + (kUnroll - 1) * nthreads < nv; q += kUnroll * nthreads) {
+        uint4 x[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) x[u] = __ldcs(s4 + q + u * nthreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) __stcs(d4 + q + u * nthreads, x[u]);
+      }
+      for (; q < nv; q += nthreads) __stcs(d4 + q, __ldcs(s4 + q));
+      done = nv * 8;
+    }
+    for (int64_t j = done + tid; j < len; j += nthreads) dst[j] = __ldcs(src + j);
+  }
+}
+
+template <int CAP>
+cudaError_t launch_rows_cap(const GatherRowsLaunch& L) {
+  GatherRowsArgs<CAP> a;
+  for (int k = 0; k < L.world; ++k) a.src[k] = L.shards[k];
+  for (int k = L.world; k < CAP; ++k) a.src[k] = nullptr;
+  a.full = L.full;
+  a.world = L.world;
+  a.ntensors = L.ntensors;
+  int64_t biggest = 1;
+  for (int i = 0; i < L.ntensors; ++i) {
+    a.rows[i] = L.rows[i];
+    a.cols[i] = L.cols[i];
+    a.per_rank[i] = L.rows_per_rank[i];
+    a.full_off[i] = L.full_off[i];
+    a.shard_off[i] = L.shard_off[i];
+    const int64_t blk = L.rows_per_rank[i] * L.cols[i];
+    if (blk > biggest) biggest = blk;
+  }
+  for (int i = L.ntensors; i < kMaxTensors; ++i)
+    a.rows[i] = a.cols[i] = a.per_rank[i] = a.full_off[i] = a.shard_off[i] = 0;
+
+  const void* kern = reinterpret_cast<const void*>(&zero3_unit_gather_rows_kernel<CAP>);
+  int sms = 0;
+  if (device_sm_count(&sms) != 0) return cudaErrorNoDevice;
+  const int64_t total = static_cast<int64_t>(sms) * gather_blocks_per_sm(kern);
+  const int64_t nseg = static_cast<int64_t>(L.ntensors) * L.world;
+  const int64_t gy = nseg < 65535 ? nseg : 65535;
+  int64_t bx = (biggest / (8 * kUnroll) + kThreads - 1) / kThreads;
+  int64_t cap = total / gy;
+  if (cap < 1) cap = 1;
+  if (bx > cap) bx = cap;
+  if (bx < 1) bx = 1;
+  dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(gy));
+  zero3_unit_gather_rows_kernel<CAP><<<grid, kThreads, 0, L.stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_unit_gather_rows(const GatherRowsLaunch& L) {
+  (void)cudaGetLastError();
+  if (L.world <= 8) return launch_rows_cap<8>(L);
+  if (L.world <= 64) return launch_rows_cap<64>(L);
+  return launch_rows_cap<1024>(L);
+}
 
 cudaError_t launch_unit_gather(const GatherLaunch& L) {
   if (L.numel <= 0) return cudaSuccess;
