@@ -510,6 +510,117 @@ def _e2e(args, rep, stream, t, dist, world_size):
             "_steps": 2 * (k_steps + 1)}
 
 
+LLAMA_LAYER = [(4096, 4096)] * 4 + [(11008, 4096), (11008, 4096), (4096, 11008), (4096, 1),
+               (4096, 1)]
+
+
+def prefetch_pass(layers, gather, compute, main_stream, side_stream):
+    """One ZeRO-3 forward pass with prefetch ("ZeRO-3 and FSDP": all-gather layer i+1's
+    parameters while layer i computes).  gather(l, slot, stream) unfolds layer l into
+    unit buffer `slot` (0 or 1); compute(l, slot) runs on the current (main) stream.
+    The gather of layer l+1 goes to the side stream as soon as the buffer it reuses
+    (layer l-1's) is free; layer l's compute waits for its own gather only."""
+    import torch
+    ev_g = [torch.cuda.Event() for _ in range(layers)]
+    ev_c = [torch.cuda.Event() for _ in range(layers)]
+    start = torch.cuda.Event()
+    start.record(main_stream)
+    side_stream.wait_event(start)
+    gather(0, 0, side_stream)
+    ev_g[0].record(side_stream)
+    for li in range(layers):
+        if li + 1 < layers:
+            if li >= 1:
+                side_stream.wait_event(ev_c[li - 1])   # slot (li+1)%2 held layer li-1
+            gather(li + 1, (li + 1) % 2, side_stream)
+            ev_g[li + 1].record(side_stream)
+        main_stream.wait_event(ev_g[li])
+        compute(li, li % 2)
+        ev_c[li].record(main_stream)
+
+
+def run_zero3_prefetch(args):
+    """ZeRO-3 forward with prefetch: L Llama-7B-layer units, FSDP2-style row-sharded over
+    N ranks.  Layer l's compute (a stand-in: one bf16 GEMM of T tokens on the unit's
+    first 4096x4096 weight) runs on the main stream while the gather of layer l+1 runs
+    on a side stream into the other of two unit buffers (the memory peak is two
+    unfolded units).  Timed serial (gather then compute on one stream) and pipelined."""
+    import torch
+    import synth
+    import zero_partitioned_mixed_adam_gb300 as za
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L, N, T = args.layers, args.prefetch_world, args.tokens
+    shard_len, U = za.rows_layout(LLAMA_LAYER, N)
+    shards = [[torch.empty(shard_len, dtype=torch.int16, device=dev) for _ in range(N)]
+              for _ in range(L)]
+    for li in range(L):
+        for r in range(N):
+            synth.fill_dev(synth.Spec(seed=li, stream=7, rank=r, sigma=0.02), 0, shard_len,
+                           synth.OUT_BF16, shards[li][r].data_ptr(), 0)
+    full = [torch.empty(U, dtype=torch.int16, device=dev) for _ in range(2)]
+    x = torch.empty(T * 4096, dtype=torch.int16, device=dev)
+    synth.fill_dev(synth.Spec(seed=99, stream=8, sigma=1.0), 0, T * 4096, synth.OUT_BF16,
+                   x.data_ptr(), 0)
+    x = x.view(torch.bfloat16).view(T, 4096)
+    y = torch.empty(T, 4096, dtype=torch.bfloat16, device=dev)
+    main_s = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+
+    def gather(li, slot, stream):
+        za.zero3_unit_gather_rows(LLAMA_LAYER, N, shards[li], full[slot], stream=stream)
+
+    def compute(li, slot):
+        w = full[slot][:4096 * 4096].view(torch.bfloat16).view(4096, 4096)
+        torch.matmul(x, w.t(), out=y)
+
+    def serial():
+        for li in range(L):
+            gather(li, 0, main_s)
+            compute(li, 0)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main_s)
+        for _ in range(args.steps):
+            fn()
+        e1.record(main_s)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps
+
+    t_g = timed(lambda: [gather(li, li % 2, main_s) for li in range(L)])
+    t_c = timed(lambda: [compute(li, li % 2) for li in range(L)])
+    t_ser = timed(serial)
+    t_pipe = timed(lambda: prefetch_pass(L, gather, compute, main_s, side))
+    peak, peak_src = _peaks()
+    g_gbs = 4 * U * L / (t_g * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": L * U / (t_pipe * 1e-3) / 1e9, "unit": "Gelem/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_pipe,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "zero3_prefetch", "layers": L, "world": N,
+                   "unit": "Llama-7B layer, 202,383,360 elements, FSDP2-style row shards",
+                   "tokens": T, "stand_in_compute": "bf16 GEMM [T,4096]x[4096,4096]^T (cuBLAS)",
+                   "buffers": "two unfolded units (double buffering)",
+                   "elements": "unit elements gathered per pass"},
+        "serial_ms": t_ser, "pipelined_ms": t_pipe, "gathers_only_ms": t_g,
+        "computes_only_ms": t_c,
+        "hidden_fraction_of_shorter": (t_ser - t_pipe) / min(t_g, t_c),
+        "roofline": {"bound": "hbm", "achieved": g_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": g_gbs / peak, "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                     "kernel": "zero3_unit_gather_rows_kernel",
+                     "algorithmic_bytes_per_launch": 4 * U, "avg_launch_ms": t_g / L},
+        "gpu_launches": L, "e2e": None, "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -521,11 +632,16 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=8, help="zero3_prefetch: units per pass")
+    ap.add_argument("--prefetch-world", type=int, default=8, help="zero3_prefetch: ranks")
+    ap.add_argument("--tokens", type=int, default=4096, help="zero3_prefetch: GEMM rows")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the workload's parameter count (smaller profiling cases)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.workload == "zero3_prefetch":
+        return run_zero3_prefetch(args)
     wl = _workload(args.workload)
     if args.numel:
         import dataclasses
