@@ -11,8 +11,8 @@
 // N*sizeof(grad) (gradients) + 12 (state read) + 12 (state write) + 2 (bf16
 // parameter) bytes and does ~20 fp32 operations: it is bound by HBM
 // bandwidth, so it is written as a streaming kernel (16-byte vector
-// loads/stores, a persistent grid-stride loop sized to the SM count) and uses
-// no tensor cores.
+// loads/stores, a persistent grid-stride loop of 512-thread blocks sized to
+// the SM count) and uses no tensor cores.
 //
 // Bit-exactness: every operation is an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nvcc cannot contract any
@@ -35,8 +35,21 @@
 namespace zeroadam {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kTableRuntime = 1024;  // gradient-pointer table of the any-N kernel
+
+// Loads.  The gradients are never written while the kernel runs, so they may
+// take the read-only (non-coherent) path.  master/m/v are read and then
+// overwritten in place, so they take the coherent path with an evict-first
+// hint: nothing is read twice.
+template <typename T>
+__device__ __forceinline__ T ld_grad(const T* p) {
+  return __ldg(p);
+}
+template <typename T>
+__device__ __forceinline__ T ld_state(const T* p) {
+  return __ldcs(p);
+}
 
 template <int CAP>
 struct StepArgs {
@@ -94,7 +107,7 @@ template <>
 struct GradVec<false> {  // 8 bf16 = one 16-byte vector
   uint4 r;
   __device__ __forceinline__ void load(const void* p, int64_t e0) {
-    r = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + e0));
+    r = ld_grad(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + e0));
   }
   __device__ __forceinline__ float get(int j) const {
     const uint32_t w = j < 2 ? r.x : j < 4 ? r.y : j < 6 ? r.z : r.w;
@@ -107,8 +120,8 @@ struct GradVec<true> {  // 8 fp32 = two 16-byte vectors
   float4 a, b;
   __device__ __forceinline__ void load(const void* p, int64_t e0) {
     const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(p) + e0);
-    a = __ldcs(q);
-    b = __ldcs(q + 1);
+    a = ld_grad(q);
+    b = ld_grad(q + 1);
   }
   __device__ __forceinline__ float get(int j) const {
     const float4& h = j < 4 ? a : b;
@@ -119,8 +132,8 @@ struct GradVec<true> {  // 8 fp32 = two 16-byte vectors
 
 template <bool GF32>
 __device__ __forceinline__ float grad_scalar(const void* p, int64_t e) {
-  if (GF32) return __ldcs(static_cast<const float*>(p) + e);
-  return bf16_to_f32(__ldcs(static_cast<const uint16_t*>(p) + e));
+  if (GF32) return ld_grad(static_cast<const float*>(p) + e);
+  return bf16_to_f32(ld_grad(static_cast<const uint16_t*>(p) + e));
 }
 
 // Sum over ranks of 8 consecutive elements.  The accumulator starts at -0.0,
@@ -163,13 +176,13 @@ __device__ __forceinline__ void sum_grads8(const StepArgs<CAP>& a, int world, in
 
 __device__ __forceinline__ void load_f32x8(const float* p, bool vec, float x[8]) {
   if (vec) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    const float4 a = ld_state(reinterpret_cast<const float4*>(p));
+    const float4 b = ld_state(reinterpret_cast<const float4*>(p) + 1);
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
   } else {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = __ldcs(p + j);
+    for (int j = 0; j < 8; ++j) x[j] = ld_state(p + j);
   }
 }
 
@@ -200,7 +213,7 @@ __device__ __forceinline__ void step_element(const StepArgs<CAP>& a, int world, 
   float acc = -0.0f;
 #pragma unroll 1
   for (int k = 0; k < world; ++k) acc = acc_add<ABF16>(acc, grad_scalar<GF32>(a.g[k], e));
-  float w = a.master[e], mm = a.m[e], vv = a.v[e];
+  float w = ld_state(a.master + e), mm = ld_state(a.m + e), vv = ld_state(a.v + e);
   adam_element(acc, a.s, w, mm, vv);
   a.master[e] = w;
   a.m[e] = mm;
