@@ -417,3 +417,36 @@ def test_7b_rank3_full_size_sampled():
     _param_is_cast_of_master(w, p[lo:hi])
     del g, w, m, v, p
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("eps", [1e-8, 0.0])
+def test_zero_gradients_and_signed_zeros(eps):
+    """Exact +-0 gradients that persist over steps (m = v = 0 stays), +-0 master weights,
+    and eps = 0 (where 0/0 must still give NaN): the kernel's zero-numerator shortcut
+    must agree with the oracle bit for bit."""
+    numel, world = 50_003, 4
+    pr = Problem(numel, world, eps=eps)
+    rng = np.random.default_rng(31)
+    zero_rows = rng.random(numel) < 0.3
+    neg = rng.random(numel) < 0.5
+    hw = pr.hw.copy()
+    hw[:numel][rng.random(numel) < 0.05] = 0.0
+    hw[:numel][rng.random(numel) < 0.05] = -0.0
+    pr.hw[:] = hw
+    pr.w.copy_(torch.from_numpy(hw).cuda())
+    lr, b1, b2, _ = pr.hp
+    for t in (1, 2, 3):
+        host = []
+        for k in range(world):
+            h = np.zeros(pr.P, np.uint16)
+            vals = oracle.f32_to_bf16(rng.normal(0, 1e-3, numel).astype(np.float32))
+            vals[zero_rows] = np.where(neg[zero_rows], 0x8000, 0x0000)
+            h[:numel] = vals
+            host.append(h)
+            pr.g[k].copy_(torch.from_numpy(h.view(np.int16)).cuda())
+        za.zero_adam_step(pr.plan, -1, list(pr.g), pr.w, pr.m, pr.v, pr.p, lr=lr, beta1=b1,
+                          beta2=b2, eps=eps, t=t)
+        oracle.zero_step(numel, world, -1, host, pr.hw, pr.hm, pr.hv, pr.hp16, lr, b1, b2, eps, t)
+        pr.check(f"zeros eps={eps} t={t}")
+    if eps == 0.0:
+        assert np.isnan(gu.to_host_f32(pr.w)[:numel][zero_rows]).all()

@@ -88,15 +88,24 @@ __device__ __forceinline__ float acc_add(float acc, float x) {
 }
 
 // Adam with bias correction on one element, in ZeroAdam.step's order.
+//
+// A zero numerator skips its division: for x > 0, (+-0) / x is exactly +-0,
+// the value the IEEE division returns.  bc1 = 1 - b1^t and bc2 = 1 - b2^t are
+// > 0 (beta in [0, 1), t >= 1); the last division is skipped only when its
+// denominator is > 0 (0 / 0 still goes through the division and gives NaN).
+// Elements whose gradient is exactly zero every step (untouched rows, dead
+// units; the GPT-2 workload's 10 % mask) keep m = v = 0, and without the
+// shortcut their divisions take the slow path of the IEEE division sequence.
 __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, float& w, float& m,
                                              float& v) {
   const float g = s.pow2_world ? __fmul_rn(gsum, s.inv_world) : __fdiv_rn(gsum, s.world);
   m = __fadd_rn(__fmul_rn(m, s.b1), __fmul_rn(s.omb1, g));
   v = __fadd_rn(__fmul_rn(v, s.b2), __fmul_rn(__fmul_rn(s.omb2, g), g));
-  const float m_hat = __fdiv_rn(m, s.bc1);
-  const float v_hat = __fdiv_rn(v, s.bc2);
+  const float m_hat = (m == 0.0f) ? m : __fdiv_rn(m, s.bc1);
+  const float v_hat = (v == 0.0f) ? v : __fdiv_rn(v, s.bc2);
   const float denom = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
-  w = __fsub_rn(w, __fdiv_rn(__fmul_rn(s.lr, m_hat), denom));
+  const float num = __fmul_rn(s.lr, m_hat);
+  w = __fsub_rn(w, (num == 0.0f && denom > 0.0f) ? num : __fdiv_rn(num, denom));
 }
 
 // 8 gradients of one rank as fp32, loaded as 16-byte vectors.
