@@ -182,7 +182,18 @@ class Replica:
         self.kernels = []
         if self.unit:
             self.kernels.append(("zero3_unit_gather_kernel", 4 * wl.numel))
-        self.kernels.append(("zero_adam_step_kernel", _bytes_per_step(wl, plan)))
+        self.kernels.append((self.step_kernel_name(), _bytes_per_step(wl, plan)))
+
+    def step_kernel_name(self):
+        """The library runs the TMA-staged kernel for N = 16 when every buffer is
+        16-byte aligned at the range's first element (whole cudaMalloc buffers)."""
+        def aligned(t, first, esize):
+            return (t.data_ptr() + first * esize) % 16 == 0
+        tma = (self.wl.world == 16 and self.n >= 8
+               and all(aligned(g, self.g_first, 2) for g in self.g)
+               and all(aligned(x, 0, 4) for x in (self.w, self.m, self.v))
+               and aligned(self.p, self.p_first, 2))
+        return "zero_adam_step_tma_kernel" if tma else "zero_adam_step_kernel"
 
     def fill_grads(self, t):
         import torch
@@ -402,10 +413,10 @@ def run_ours(args, wl):
     dom = max(per_kernel, key=lambda k: k["avg_launch_ms"] * 1)
     peak, peak_src = _peaks()
     traffic = None
-    if dom["kernel"] == "zero_adam_step_kernel":
+    if dom["kernel"].startswith("zero_adam_step"):
         rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc",
                                            "adam_step.cu"))
-        if rec and rec.get("world") == wl.world:
+        if rec and rec.get("world") == wl.world and rec.get("kernel", dom["kernel"]) == dom["kernel"]:
             traffic = rec["dram_bytes_per_element"] * rep.n
 
     e2e = None

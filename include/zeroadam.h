@@ -57,6 +57,7 @@ extern "C" {
 #define ZERO_E_DEVICE (-12) /* no usable CUDA device                                */
 #define ZERO_E_RANGE (-13)  /* zero_adam_step_range: begin < 0 or end < begin       */
 #define ZERO_E_SHAPE (-14)  /* zero3_unit_gather_rows: bad tensor count or shape    */
+#define ZERO_E_TIMEOUT (-15) /* a kernel gave up a bounded wait (zero_device_status) */
 
 /* Largest tensor count of one zero3_unit_gather_rows unit. */
 #define ZERO_MAX_UNIT_TENSORS 256
@@ -224,6 +225,19 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
                            void* stream);
 
 /* ------------------------------------------------------------------ misc */
+
+/*
+ * Device-side status of the library's kernels on the current device.  Some
+ * launches stage data through shared memory with asynchronous bulk copies and
+ * wait on hardware barriers; every such wait is bounded, and a wait that gives
+ * up (seconds without progress) ends the launch early, leaving that step's
+ * outputs incomplete, and records the fact in a per-device status word.
+ * Returns ZERO_OK if no wait has given up since the previous call, else
+ * ZERO_E_TIMEOUT; either way the word is cleared.  ZERO_E_DEVICE if there is no
+ * usable device.  Unlike the other calls this one synchronises the current
+ * device (it reads device memory).
+ */
+int zero_device_status(void);
 
 /* Text for a status code.  For ZERO_E_LAUNCH it includes the CUDA error text
    of this thread's last failed launch.  The pointer stays valid until this

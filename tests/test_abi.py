@@ -217,6 +217,12 @@ def test_gather_rows_argument_errors(za):
     assert za.rows_layout([(10, 3), (7, 2)], 4) == (3 * 3 + 2 * 2, 44)
 
 
+def test_device_status_without_a_gpu(za):
+    # no CUDA device in this process: the call reports it instead of failing
+    if not __import__("conftest").cuda_available():
+        assert za.device_status() == -12
+
+
 def test_strerror(za):
     for code in za.ERRORS:
         s = za.strerror(code)

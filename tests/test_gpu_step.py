@@ -450,3 +450,23 @@ def test_zero_gradients_and_signed_zeros(eps):
         pr.check(f"zeros eps={eps} t={t}")
     if eps == 0.0:
         assert np.isnan(gu.to_host_f32(pr.w)[:numel][zero_rows]).all()
+
+
+@pytest.mark.parametrize("numel", [8, 13, 2048 * 16 + 8, 2048 * 152 * 2 + 5, 4_000_037])
+def test_world16_staged_path_sizes(numel):
+    """N = 16 with aligned buffers takes the TMA-staged kernel: partial last tiles,
+    fewer tiles than SMs, a scalar tail; two steps against the oracle, and the
+    device status word stays clear."""
+    pr = Problem(numel, 16, seed=numel % 11)
+    for t in (1, 2):
+        pr.step(t)
+        pr.check(f"N=16 {numel} t={t}")
+    assert za.device_status() == 0
+
+
+@pytest.mark.parametrize("offs", [(1, 0, 0), (0, 1, 0), (0, 0, 3)])
+def test_world16_misaligned_falls_back(offs):
+    pr = Problem(100_003, 16, offs=offs)
+    pr.step(1)
+    pr.check(f"N=16 offs {offs}")
+    assert za.device_status() == 0

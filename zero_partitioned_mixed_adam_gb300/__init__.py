@@ -28,12 +28,12 @@ ERRORS = {
     -1: "ZERO_E_NULLPTR", -2: "ZERO_E_WORLD", -3: "ZERO_E_NUMEL", -4: "ZERO_E_RANK",
     -5: "ZERO_E_STEP", -6: "ZERO_E_ALIGN", -7: "ZERO_E_HPARAM", -8: "ZERO_E_LAYOUT",
     -9: "ZERO_E_PLAN", -10: "ZERO_E_ALIAS", -11: "ZERO_E_LAUNCH", -12: "ZERO_E_DEVICE",
-    -13: "ZERO_E_RANGE", -14: "ZERO_E_SHAPE",
+    -13: "ZERO_E_RANGE", -14: "ZERO_E_SHAPE", -15: "ZERO_E_TIMEOUT",
 }
 
 # Every symbol include/zeroadam.h declares.
 EXPORTS = ("zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero3_unit_gather_rows", "zero_strerror", "zero_version")
+           "zero3_unit_gather_rows", "zero_device_status", "zero_strerror", "zero_version")
 
 
 class ZeroError(RuntimeError):
@@ -81,6 +81,8 @@ def _load() -> ctypes.CDLL:
     lib.zero3_unit_gather.restype = ctypes.c_int
     lib.zero3_unit_gather_rows.argtypes = [i32, vp, vp, i32, vp, vp, vp]
     lib.zero3_unit_gather_rows.restype = ctypes.c_int
+    lib.zero_device_status.argtypes = []
+    lib.zero_device_status.restype = ctypes.c_int
     lib.zero_strerror.argtypes = [ctypes.c_int]
     lib.zero_strerror.restype = ctypes.c_char_p
     lib.zero_version.argtypes = []
@@ -195,6 +197,12 @@ def zero3_unit_gather_rows(shapes, world: int, shards, full, stream=None) -> Non
         raise ZeroError(rc, "zero3_unit_gather_rows")
 
 
+def device_status() -> int:
+    """ZERO_OK, or ZERO_E_TIMEOUT if a kernel gave up a bounded wait since the last call
+    (clears the word; synchronises the current device)."""
+    return _lib.zero_device_status()
+
+
 def version() -> int:
     return _lib.zero_version()
 
@@ -205,7 +213,7 @@ def raw_lib() -> ctypes.CDLL:
 
 
 __all__ = ["zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero3_unit_gather_rows", "rows_layout",
+           "zero3_unit_gather_rows", "rows_layout", "device_status",
            "ZeroPlan", "ZeroError", "strerror", "version", "raw_lib", "ZERO_ALL_RANKS",
            "ZERO_GRAD_FULL", "ZERO_GRAD_SHARD", "ZERO_GRAD_WINDOW", "ZERO_GRAD_F32",
            "ZERO_ACC_BF16", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "EXPORTS", "LIB_PATH"]

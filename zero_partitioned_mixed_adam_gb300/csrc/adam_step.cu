@@ -79,6 +79,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
          (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
 }
 
+// acc[j] += element j of one 16-byte vector of 8 bf16 (fp32 sum).
+__device__ __forceinline__ void accumulate_bf16x8(float acc[8], const uint4 r) {
+  acc[0] = __fadd_rn(acc[0], bf16_lo(r.x));
+  acc[1] = __fadd_rn(acc[1], bf16_hi(r.x));
+  acc[2] = __fadd_rn(acc[2], bf16_lo(r.y));
+  acc[3] = __fadd_rn(acc[3], bf16_hi(r.y));
+  acc[4] = __fadd_rn(acc[4], bf16_lo(r.z));
+  acc[5] = __fadd_rn(acc[5], bf16_hi(r.z));
+  acc[6] = __fadd_rn(acc[6], bf16_lo(r.w));
+  acc[7] = __fadd_rn(acc[7], bf16_hi(r.w));
+}
+
+__device__ __forceinline__ void unpack8(const float4 a, const float4 b, float x[8]) {
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
 // One step of the running sum over ranks.
 template <bool ABF16>
 __device__ __forceinline__ float acc_add(float acc, float x) {
@@ -256,6 +273,223 @@ __global__ void __launch_bounds__(kThreads)
     step_element<NT, CAP, GF32, ABF16>(a, world, e);
 }
 
+// ---------------------------------------------------------------------------
+// TMA-staged variant for N = 16, bf16 gradients, fp32 sum (measured faster
+// than the register-staged kernel there; at N = 8 it is not, so it is not used).
+// One CTA per SM.  Warp 0 lane 0 is the producer: for each 2048-element tile
+// it issues one bulk copy (cp.async.bulk, the TMA engine) per rank's gradient
+// tile and per state array into a two-stage shared-memory ring, and the
+// stage's mbarrier completes when all bytes have landed.  Warps 1..8 consume:
+// each thread sums its 8 elements over the ranks and runs adam_element from
+// shared memory, then stores to global.  Every wait is bounded; a wait that
+// gives up records a nonzero status in g_step_status (read by
+// zero_device_status), the producer waits (bounded) for its own copies, and
+// every thread returns.
+
+constexpr int kTmaTile = 2048;       // elements per tile
+constexpr int kTmaConsumers = 256;   // 8 warps, 8 elements per thread
+constexpr int kTmaStages = 2;
+constexpr uint32_t kTmaSpin = 1u << 22;  // try_wait polls before a wait gives up
+
+__device__ int g_step_status;
+
+template <int NT>
+struct TmaArgs {
+  const uint16_t* g[NT];
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* param;
+  int64_t n;      // elements in the range
+  int64_t nbody;  // multiple of 8: [0, nbody) through the ring, [nbody, n) scalar
+  AdamScalars s;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+// Bounded wait for the completion of the barrier phase of the given parity.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+  for (uint32_t i = 0; i < kTmaSpin; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+// 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.  Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(b))
+      : "memory");
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kTmaConsumers + 32, 1)
+    zero_adam_step_tma_kernel(const __grid_constant__ TmaArgs<NT> a) {
+  // stage: NT bf16 gradient tiles, then the master, m and v fp32 tiles
+  constexpr int64_t kGradBytes = kTmaTile * 2;
+  constexpr int64_t kStage = NT * kGradBytes + 3 * kTmaTile * 4;
+  extern __shared__ __align__(1024) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kTmaStages], empty[kTmaStages];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t ntiles = (a.nbody + kTmaTile - 1) / kTmaTile;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTmaStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kTmaConsumers / 32);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane != 0) return;
+    int64_t k = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+      const int s = static_cast<int>(k % kTmaStages);
+      if (k >= kTmaStages &&
+          !mbar_wait(&empty[s], static_cast<uint32_t>((k / kTmaStages - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const int64_t e0 = tile * kTmaTile;
+      int64_t cnt = a.nbody - e0;
+      if (cnt > kTmaTile) cnt = kTmaTile;
+      const uint32_t gbytes = static_cast<uint32_t>(cnt * 2);
+      uint8_t* st = ring + s * kStage;
+      mbar_expect_tx(&full[s], gbytes * NT + 3 * 2 * gbytes);
+      for (int r = 0; r < NT; ++r) bulk_load(st + r * kGradBytes, a.g[r] + e0, gbytes, &full[s]);
+      uint8_t* sf = st + NT * kGradBytes;
+      bulk_load(sf, a.master + e0, 2 * gbytes, &full[s]);
+      bulk_load(sf + kTmaTile * 4, a.m + e0, 2 * gbytes, &full[s]);
+      bulk_load(sf + 2 * kTmaTile * 4, a.v + e0, 2 * gbytes, &full[s]);
+    }
+    if (!ok) {
+      atomicExch(&g_step_status, 1);
+      const int64_t first = k > kTmaStages ? k - kTmaStages : 0;
+      for (int64_t j = first; j < k; ++j)
+        mbar_wait(&full[j % kTmaStages], static_cast<uint32_t>((j / kTmaStages) & 1));
+    }
+    return;
+  }
+
+  const int t = threadIdx.x - 32;
+  int64_t k = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = static_cast<int>(k % kTmaStages);
+    if (!mbar_wait(&full[s], static_cast<uint32_t>((k / kTmaStages) & 1))) {
+      atomicExch(&g_step_status, 2);
+      return;
+    }
+    const int64_t e0 = tile * kTmaTile + 8 * t;
+    const bool in = e0 < a.nbody;  // e0 and nbody are multiples of 8
+    const uint8_t* st = ring + s * kStage;
+    float acc[8], w[8], mm[8], vv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = -0.0f;
+    if (in) {
+#pragma unroll
+      for (int r = 0; r < NT; ++r)
+        accumulate_bf16x8(acc, *reinterpret_cast<const uint4*>(st + r * kGradBytes + 16 * t));
+      const float4* sf = reinterpret_cast<const float4*>(st + NT * kGradBytes);
+      unpack8(sf[2 * t], sf[2 * t + 1], w);
+      unpack8(sf[kTmaTile / 4 + 2 * t], sf[kTmaTile / 4 + 2 * t + 1], mm);
+      unpack8(sf[kTmaTile / 2 + 2 * t], sf[kTmaTile / 2 + 2 * t + 1], vv);
+    }
+    // every lane has read its slice of stage s: the warp hands the stage back
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (in) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) adam_element(acc[j], a.s, w[j], mm[j], vv[j]);
+      store_f32x8(a.master + e0, true, w);
+      store_f32x8(a.m + e0, true, mm);
+      store_f32x8(a.v + e0, true, vv);
+      store_bf16x8_rn(a.param + e0, true, w);
+    }
+  }
+  // the last few (< 8) elements of the range, one per thread of block 0
+  if (blockIdx.x == 0 && a.nbody + t < a.n) {
+    const int64_t e = a.nbody + t;
+    float acc = -0.0f;
+#pragma unroll
+    for (int r = 0; r < NT; ++r) acc = __fadd_rn(acc, bf16_to_f32(ld_grad(a.g[r] + e)));
+    float w = ld_state(a.master + e), mm = ld_state(a.m + e), vv = ld_state(a.v + e);
+    adam_element(acc, a.s, w, mm, vv);
+    a.master[e] = w;
+    a.m[e] = mm;
+    a.v[e] = vv;
+    a.param[e] = f32_to_bf16_rn(w);
+  }
+}
+
+constexpr size_t tma_smem_bytes(int nt) {
+  return static_cast<size_t>(kTmaStages) * (nt * kTmaTile * 2 + 3 * kTmaTile * 4);
+}
+
+// Launch the TMA kernel when every buffer is 16-byte aligned at the range's
+// first element (head == 0 with all streams vectorised).  Returns false when
+// the variant does not apply.
+template <int NT>
+bool launch_tma(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* err) {
+  if (!(a.head == 0 && a.gvec && a.svec && a.pvec) || a.nvec < 1) return false;
+  static std::mutex mu;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(zero_adam_step_tma_kernel<NT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tma_smem_bytes(NT))) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+      }
+      configured[dev] = true;
+    }
+  }
+  int sms = 0;
+  if (device_sm_count(&sms) != 0) return false;
+  TmaArgs<NT> t;
+  for (int k = 0; k < NT; ++k) t.g[k] = static_cast<const uint16_t*>(L.grads[k]);
+  t.master = L.master;
+  t.m = L.m;
+  t.v = L.v;
+  t.param = L.param;
+  t.n = L.n;
+  t.nbody = 8 * a.nvec;
+  t.s = L.s;
+  const int64_t ntiles = (t.nbody + kTmaTile - 1) / kTmaTile;
+  const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
+  zero_adam_step_tma_kernel<NT>
+      <<<grid, kTmaConsumers + 32, tma_smem_bytes(NT), L.stream>>>(t);
+  *err = cudaGetLastError();
+  return true;
+}
+
 // Resident blocks per SM of a kernel on the current device (cached).
 int blocks_per_sm(const void* kernel) {
   static std::mutex mu;
@@ -320,6 +554,11 @@ cudaError_t launch_world(const StepLaunch& L) {
   a.svec = (rs >= 0 && (rs + best_h) % 4 == 0);
   a.pvec = ((rp + best_h) % 8 == 0);
 
+  if constexpr (NT == 16 && CAP == 16 && !GF32 && !ABF16) {
+    cudaError_t err = cudaSuccess;
+    if (launch_tma<16>(L, a, &err)) return err;
+  }
+
   const void* kern = reinterpret_cast<const void*>(&zero_adam_step_kernel<NT, CAP, GF32, ABF16>);
   int sms = 0;
   if (device_sm_count(&sms) != 0) return cudaErrorNoDevice;
@@ -347,6 +586,17 @@ cudaError_t launch_variant(const StepLaunch& L) {
 }
 
 }  // namespace
+
+int read_and_clear_step_status(int* status) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_step_status, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_step_status, &zero, sizeof(int)) != cudaSuccess) return -1;
+  }
+  *status = v;
+  return 0;
+}
 
 cudaError_t launch_adam_step(const StepLaunch& L) {
   if (L.n <= 0) return cudaSuccess;

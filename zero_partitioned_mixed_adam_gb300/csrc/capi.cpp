@@ -299,6 +299,14 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
   return launch_status(launch_unit_gather_rows(L));
 }
 
+int zero_device_status(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_E_DEVICE;
+  int word = 0;
+  if (read_and_clear_step_status(&word) != 0) return ZERO_E_DEVICE;
+  return word == 0 ? ZERO_OK : ZERO_E_TIMEOUT;
+}
+
 const char* zero_strerror(int status) {
   switch (status) {
     case ZERO_OK: return "ok";
@@ -315,6 +323,7 @@ const char* zero_strerror(int status) {
     case ZERO_E_DEVICE: return "no usable CUDA device";
     case ZERO_E_RANGE: return "the window must satisfy 0 <= begin <= end";
     case ZERO_E_SHAPE: return "ntensors in [1, ZERO_MAX_UNIT_TENSORS] and sizes >= 1 required";
+    case ZERO_E_TIMEOUT: return "a kernel gave up a bounded wait; that step's outputs are incomplete";
     case ZERO_E_LAUNCH:
       t_msg = std::string("kernel launch failed: ") + cudaGetErrorString(t_last_cuda);
       return t_msg.c_str();

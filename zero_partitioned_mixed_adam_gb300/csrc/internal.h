@@ -66,6 +66,9 @@ struct GatherRowsLaunch {
 int device_sm_count(int* sms);
 
 cudaError_t launch_adam_step(const StepLaunch& L);
+// Status word of the step kernels' bounded waits on the current device (0 =
+// every wait completed); read and cleared.  Returns -1 if CUDA fails.
+int read_and_clear_step_status(int* status);
 cudaError_t launch_unit_gather(const GatherLaunch& L);
 cudaError_t launch_unit_gather_rows(const GatherRowsLaunch& L);
 
