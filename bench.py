@@ -616,6 +616,15 @@ def run_zero2_buckets(args):
         return e0.elapsed_time(e1) / args.steps
 
     t_whole, t_buckets = timed(whole), timed(buckets_only)
+    # the same bucket steps replayed from a CUDA graph (no per-launch host work)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i, b0 in enumerate(starts):
+                step_bucket(i, b0, cap)
+    t_graph = timed(graph.replay)
     t_bwd, t_serial, t_over = timed(backward_only), timed(backward_then_steps), timed(overlapped)
     peak, peak_src = _peaks()
     nbytes = (2 * N + 26) * numel
@@ -630,6 +639,7 @@ def run_zero2_buckets(args):
                    "value": "parameters per overlapped backward+step pass"},
         "whole_step_ms": t_whole, "bucket_steps_ms": t_buckets,
         "small_launch_efficiency": t_whole / t_buckets,
+        "bucket_steps_graph_ms": t_graph, "small_launch_efficiency_graph": t_whole / t_graph,
         "backward_only_ms": t_bwd, "backward_then_steps_ms": t_serial,
         "overlapped_ms": t_over,
         "hidden_fraction_of_steps": (t_serial - t_over) / t_buckets,
