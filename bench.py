@@ -452,6 +452,17 @@ def run_ours(args, wl):
     return 0
 
 
+def _host_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def _e2e(args, rep, stream, t, dist, world_size):
     """The same step through the public API with HOST buffers.  Every step's inputs
     (the N ranks' gradients; for ZeRO-3 units also the N parameter shards) sit in
@@ -465,6 +476,22 @@ def _e2e(args, rep, stream, t, dist, world_size):
     k_steps = max(1, min(args.steps, args.e2e_steps))
     n = rep.n
     g_len = rep.g[0].numel()
+    # every rank on this host pins its own copy: keep the total within half of what is free
+    need = 2 * g_len * wl.world + 2 * rep.p.numel()
+    if rep.unit:
+        need += sum(2 * x.numel() for x in rep.shards)
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    avail = _host_available_bytes()
+    skip = avail is not None and need * local_ranks > 0.5 * avail
+    if dist is not None:   # one decision for all ranks (they meet in barriers below)
+        flag = torch.tensor([1.0 if skip else 0.0], device=rep.dev)
+        dist.all_reduce(flag, op=dist.ReduceOp.MAX)
+        skip = flag.item() > 0
+    if skip:
+        return {"value": None, "unit": "Gelem/s", "h2d_bytes_per_step": 2 * n * wl.world,
+                "d2h_bytes_per_step": 2 * n, "skipped": (
+                    f"{local_ranks} ranks x {need / 1e9:.1f} GB of pinned host buffers exceed half "
+                    f"of the host memory available"), "_steps": 0}
     hg = [torch.empty(g_len, dtype=torch.int16, pin_memory=True) for _ in range(wl.world)]
     for k in range(wl.world):
         hg[k].copy_(rep.g[k])

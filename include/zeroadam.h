@@ -16,9 +16,15 @@
  *
  * Conventions for every call:
  *   - Status: 0 (ZERO_OK) or a negative ZERO_E_* code.  Nothing is launched
- *     when a call returns an error.  No call aborts, allocates device memory,
- *     synchronises, or keeps state between calls.  Faults inside a launched
- *     kernel surface, as for any CUDA work, at the caller's next sync.
+ *     when a call returns an error.  No call aborts or allocates device
+ *     memory; none synchronises except zero_device_status; the only state kept
+ *     between calls is a per-device status word that a kernel sets only if one
+ *     of its bounded waits gives up (see zero_device_status).  Faults inside a
+ *     launched kernel surface, as for any CUDA work, at the caller's next sync.
+ *   - Calls on different streams may run concurrently when their output
+ *     buffers are disjoint; a sequence of calls may be captured into a CUDA
+ *     graph after each kernel's first call on the device (which does one-time
+ *     set-up outside any capture).
  *   - Device pointers are in the current CUDA device's address space; the
  *     stream argument is a cudaStream_t passed as void* (NULL = the legacy
  *     default stream) and must belong to the current device.

@@ -55,7 +55,7 @@ int make_plan(int64_t numel, int32_t world, zero_plan_t* p) {
   const int64_t shard = numel / world + (numel % world != 0 ? 1 : 0);
   if (shard > INT64_MAX / world) return ZERO_E_NUMEL;
   const int64_t padded = shard * world;
-  // bytes_* must fit in uint64: 16*numel <= 16*INT64_MAX < 2^68 could overflow
+  // the byte counts below (at most 16 * numel) must not overflow
   if (numel > INT64_MAX / 16) return ZERO_E_NUMEL;
   p->numel = numel;
   p->world = world;
