@@ -416,7 +416,8 @@ def run_ours(args, wl):
     if dom["kernel"].startswith("zero_adam_step"):
         rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc",
                                            "adam_step.cu"))
-        if rec and rec.get("world") == wl.world and rec.get("kernel", dom["kernel"]) == dom["kernel"]:
+        rec = (rec or {}).get(f"{dom['kernel']}/N{wl.world}")
+        if rec:
             traffic = rec["dram_bytes_per_element"] * rep.n
 
     e2e = None

@@ -54,15 +54,23 @@ def test_ranks_on_concurrent_streams(world):
     assert _same((w, m, v, p), ref)
 
 
-def test_bucket_sequence_captured_in_a_cuda_graph():
-    numel, world, bucket = 3_000_017, 8, 1 << 18
+@pytest.mark.parametrize("world", [8, 16])
+def test_bucket_sequence_captured_in_a_cuda_graph(world):
+    """Bucket steps (register-staged kernel at N = 8, TMA-staged at N = 16) and a unit
+    gather, captured together and replayed."""
+    numel, bucket = 3_000_017, 1 << 18
     plan, g, w0 = _setup(numel, world)
     starts = list(range(0, numel, bucket))[::-1]
+    uplan = za.zero_plan(1_000_003, world)
+    shards = [torch.full((uplan.shard,), k, dtype=torch.int16, device="cuda")
+              for k in range(world)]
+    full = torch.zeros(1_000_003, dtype=torch.int16, device="cuda")
 
     def run(state, t, stream=None):
         for b0 in starts:
             za.zero_adam_step_range(plan, -1, b0, b0 + bucket, g, *state, lr=1e-3, t=t,
                                     grad_layout=za.ZERO_GRAD_FULL, stream=stream)
+        za.zero3_unit_gather(uplan, shards, full, stream=stream)
 
     graphed = [w0.clone(), torch.zeros_like(w0), torch.zeros_like(w0),
                torch.zeros(numel, dtype=torch.int16, device="cuda")]
@@ -82,4 +90,5 @@ def test_bucket_sequence_captured_in_a_cuda_graph():
         run(eager2, t)
     torch.cuda.synchronize()
     assert _same(check, eager2)
+    assert torch.equal(full, torch.cat(shards)[:1_000_003])
     assert za.device_status() == 0
