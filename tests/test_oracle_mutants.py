@@ -51,6 +51,9 @@ MUTANTS = {
                                    "    shard_off += (rows[i] / world) * cols[i];"),
     "rows_local_row_from_next_rank": ("      const int64_t local = row - r * R;",
                                       "      const int64_t local = row - r * R + (r > 0 ? 1 : 0);"),
+    "no_bias_correction_v": ("const float v_hat = vv / s->bc2;", "const float v_hat = vv;"),
+    "param_from_old_master": ("  ww = ww - upd;\n\n  *m = mm;\n  *v = vv;\n  *w = ww;\n  *p = oracle_f32_to_bf16(ww);",
+                              "  *p = oracle_f32_to_bf16(ww);\n  ww = ww - upd;\n\n  *m = mm;\n  *v = vv;\n  *w = ww;"),
     "zero3_one_gather": ("out->comm_z3 = all_gather + all_gather + reduce_scatter;",
                          "out->comm_z3 = all_gather + reduce_scatter;"),
     "ring_share_whole_vector": ("const double ring_share = ((double)world - 1.0) / (double)world;",
