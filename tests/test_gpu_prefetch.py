@@ -8,7 +8,6 @@ import torch
 import oracle
 import synth
 from conftest import cuda_available
-import gpu_util as gu
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
