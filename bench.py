@@ -5,8 +5,10 @@ One step = one call of zero_adam_step over every rank's shard (or one rank's,
 for the single-rank workload): the emulated reduce-scatter of the N ranks' bf16
 gradients, bias-corrected Adam on the fp32 master/m/v, and the bf16 cast into
 the flat parameter buffer.  Inputs are seeded and synthetic (synth/), resident
-in HBM before timing; every workload moves far more than the 129 MB L2 per
-step, so no L2 flush is needed between steps.
+in HBM before timing.  A workload that moves at least four L2 sizes per step
+(every default one) runs its timed steps back to back; a smaller one (tiny, the
+small ZeRO-3 units) has the L2 flushed before every timed step, outside the
+timed launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -235,6 +237,30 @@ class Replica:
         return sum(b for _, b in self.kernels)
 
 
+class L2Flush:
+    """Evicts the L2 between timed steps of a workload that moves less than a few L2
+    sizes per step: a write of twice the L2, then a read of another such buffer, so
+    that the next step starts with clean lines (no write-backs charged to it)."""
+
+    def __init__(self, dev):
+        import torch
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
+        self.nbytes = 2 * l2
+        self.a = torch.empty(self.nbytes // 4, dtype=torch.float32, device=dev)
+        self.b = torch.zeros(self.nbytes // 4, dtype=torch.float32, device=dev)
+        self.l2 = l2
+
+    def __call__(self, i):
+        self.a.fill_(float(i & 7))
+        self.b.sum()
+
+    @staticmethod
+    def needed(step_bytes, dev):
+        import torch
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
+        return step_bytes < 4 * l2
+
+
 class OracleSample:
     """The oracle (plain C) on a window of the workload, run over all host cores as
     disjoint sub-windows.  Inputs are generated once; each call steps the window."""
@@ -283,6 +309,23 @@ class OracleSample:
             if el >= seconds:
                 return done / el, done // self.n, el
 
+    def timed_single_thread(self, seconds, elems=1 << 18):
+        """The plain oracle on one host thread, over the first `elems` of the window."""
+        import oracle
+        wl, a = self.wl, self.a
+        n = min(elems, self.n)
+        done, t0 = 0, time.perf_counter()
+        while True:
+            self.t += 1
+            oracle.zero_step(wl.numel, wl.world, -1 if wl.rank < 0 else wl.rank, self.grads,
+                             self.hw, self.hm, self.hv, self.hp, wl.lr, wl.beta1, wl.beta2,
+                             wl.eps, self.t, i0=a, i1=a + n, grad_base=a, state_base=a,
+                             param_base=a)
+            done += n
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return done / el
+
     def describe(self, reps, secs):
         return (f"window [{self.a}, {self.b}) of {self.wl.name} ({self.n} elements x "
                 f"{self.wl.world} ranks), stepped {reps} times in {secs:.1f} s on "
@@ -293,8 +336,11 @@ def _cpu_oracle_sample(wl, seconds):
     s = OracleSample(wl)
     s.step()  # warm
     rate, reps, secs = s.timed(seconds)
+    one = s.timed_single_thread(min(3.0, seconds))
     return {"value": rate / 1e9, "unit": "Gelem/s", "cores": s.cores, "kind": "oracle",
-            "sample": s.describe(reps, secs)}
+            "sample": s.describe(reps, secs), "single_thread_value": one / 1e9,
+            "single_thread_sample": f"first {min(1 << 18, s.n)} elements of the window, "
+                                    "one host thread"}
 
 
 def run_reference(args, wl):
@@ -341,11 +387,16 @@ def aggregate(ms_local: float, elems_per_rank: int, world_size: int, dist=None, 
     return ms, world_size * elems_per_rank / (ms * 1e-3) / 1e9
 
 
-def _config(wl, rep):
+def _config(wl, rep, flush=None):
+    l2 = "inputs larger than L2 (no flush)"
+    if flush is not None:
+        l2 = (f"L2 flushed before every timed step: a {flush.nbytes >> 20} MiB write, then a "
+              f"{flush.nbytes >> 20} MiB read (clean lines), outside the timed launches; "
+              "ms_per_step is the sum of the step's launch times")
     c = {"workload": wl.name, "numel": wl.numel, "world": wl.world,
          "rank": "all" if wl.rank < 0 else wl.rank, "grad_layout": wl.grad_layout,
          "param_layout": wl.param_layout, "grad_dist": ["normal", "student_t3"][wl.grad_dist],
-         "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas",
+         "l2": l2, "parallelism": "replicas",
          "state": "fp32 master/m/v, bf16 grads and params"}
     if rep is not None:
         c["shard"] = rep.plan.shard
@@ -386,6 +437,7 @@ def run_ours(args, wl):
     nk = len(rep.kernels)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(nk)] for _ in range(args.steps)]
+    flush = L2Flush(dev) if L2Flush.needed(rep.step_bytes(), dev) else None
     sampler = ClockSampler(local)
     sampler.start()
     if dist is not None:
@@ -394,13 +446,18 @@ def run_ours(args, wl):
     t_wall = time.perf_counter()
     for i in range(args.steps):
         t += 1
+        if flush is not None:
+            flush(i)
         rep.step(t, stream, ev[i])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t_wall
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
-    total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1])
+    if flush is None:
+        total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1])
+    else:   # the flushes sit between the steps: add up the steps' own launches
+        total_ms = sum(e0.elapsed_time(e1) for step in ev for e0, e1 in step)
     per_kernel = []
     for j, (name, nbytes) in enumerate(rep.kernels):
         ms = [ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps)]
@@ -434,7 +491,7 @@ def run_ours(args, wl):
             "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": world_size,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": _config(wl, rep),
+            "data": "synthetic", "config": _config(wl, rep, flush),
             "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak,
             "roofline": {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                          "frac": dom["gbs"] / peak, "traffic": traffic,
