@@ -187,15 +187,18 @@ class Replica:
         self.kernels.append((self.step_kernel_name(), _bytes_per_step(wl, plan)))
 
     def step_kernel_name(self):
-        """The library runs the TMA-staged kernel for N = 16 when every buffer is
-        16-byte aligned at the range's first element (whole cudaMalloc buffers)."""
+        """The library runs a TMA-staged kernel for N = 16 (gradients and state
+        staged) and N = 8 (gradients staged) when every buffer is 16-byte aligned
+        at the range's first element (whole cudaMalloc buffers)."""
         def aligned(t, first, esize):
             return (t.data_ptr() + first * esize) % 16 == 0
-        tma = (self.wl.world == 16 and self.n >= 8
+        tma = (self.wl.world in (8, 16) and self.n >= 8
                and all(aligned(g, self.g_first, 2) for g in self.g)
                and all(aligned(x, 0, 4) for x in (self.w, self.m, self.v))
                and aligned(self.p, self.p_first, 2))
-        return "zero_adam_step_tma_kernel" if tma else "zero_adam_step_kernel"
+        if not tma:
+            return "zero_adam_step_kernel"
+        return "zero_adam_step_tma_kernel" if self.wl.world == 16 else "zero_adam_step_tma_grad_kernel"
 
     def fill_grads(self, t):
         import torch

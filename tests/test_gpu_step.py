@@ -452,21 +452,28 @@ def test_zero_gradients_and_signed_zeros(eps):
         assert np.isnan(gu.to_host_f32(pr.w)[:numel][zero_rows]).all()
 
 
-@pytest.mark.parametrize("numel", [8, 13, 2048 * 16 + 8, 2048 * 152 * 2 + 5, 4_000_037])
-def test_world16_staged_path_sizes(numel):
-    """N = 16 with aligned buffers takes the TMA-staged kernel: partial last tiles,
-    fewer tiles than SMs, a scalar tail; two steps against the oracle, and the
-    device status word stays clear."""
-    pr = Problem(numel, 16, seed=numel % 11)
+# TMA-staged kernel tiles: 2048 elements at N = 16, 3072 at N = 8
+STAGED = ([(16, n) for n in (8, 13, 2048 * 16 + 8, 2048 * 152 * 2 + 5, 4_000_037)]
+          + [(8, n) for n in (8, 13, 3072 * 8 + 8, 3072 * 152 * 3 + 5, 3072 * 152 + 3072 - 8,
+                              4_000_037)])
+
+
+@pytest.mark.parametrize("world,numel", STAGED)
+def test_staged_path_sizes(world, numel):
+    """N = 16 and N = 8 with aligned buffers take the TMA-staged kernels (gradients
+    and state staged at N = 16, gradients only at N = 8): partial last tiles, fewer tiles than SMs, more tiles than SMs with a ragged last round, a
+    scalar tail; two steps against the oracle, and the device status word stays clear."""
+    pr = Problem(numel, world, seed=numel % 11)
     for t in (1, 2):
         pr.step(t)
-        pr.check(f"N=16 {numel} t={t}")
+        pr.check(f"N={world} {numel} t={t}")
     assert za.device_status() == 0
 
 
+@pytest.mark.parametrize("world", [8, 16])
 @pytest.mark.parametrize("offs", [(1, 0, 0), (0, 1, 0), (0, 0, 3)])
-def test_world16_misaligned_falls_back(offs):
-    pr = Problem(100_003, 16, offs=offs)
+def test_staged_misaligned_falls_back(world, offs):
+    pr = Problem(100_003, world, offs=offs)
     pr.step(1)
-    pr.check(f"N=16 offs {offs}")
+    pr.check(f"N={world} offs {offs}")
     assert za.device_status() == 0

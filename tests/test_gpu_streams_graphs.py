@@ -54,10 +54,10 @@ def test_ranks_on_concurrent_streams(world):
     assert _same((w, m, v, p), ref)
 
 
-@pytest.mark.parametrize("world", [8, 16])
+@pytest.mark.parametrize("world", [4, 8, 16])
 def test_bucket_sequence_captured_in_a_cuda_graph(world):
-    """Bucket steps (register-staged kernel at N = 8, TMA-staged at N = 16) and a unit
-    gather, captured together and replayed."""
+    """Bucket steps (register-staged kernel at N = 4, TMA-staged at N = 8 and 16) and a
+    unit gather, captured together and replayed."""
     numel, bucket = 3_000_017, 1 << 18
     plan, g, w0 = _setup(numel, world)
     starts = list(range(0, numel, bucket))[::-1]

@@ -12,7 +12,9 @@
 // parameter) bytes and does ~20 fp32 operations: it is bound by HBM
 // bandwidth, so it is written as a streaming kernel (16-byte vector
 // loads/stores, a persistent grid-stride loop of 512-thread blocks sized to
-// the SM count) and uses no tensor cores.
+// the SM count) and uses no tensor cores.  For N = 16 and N = 8 with aligned
+// buffers, TMA-staged variants (bulk copies into a shared-memory ring, one
+// CTA per SM) replace it.
 //
 // Bit-exactness: every operation is an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nvcc cannot contract any
@@ -275,7 +277,9 @@ __global__ void __launch_bounds__(kThreads)
 
 // ---------------------------------------------------------------------------
 // TMA-staged variant for N = 16, bf16 gradients, fp32 sum (measured faster
-// than the register-staged kernel there; at N = 8 it is not, so it is not used).
+// than the register-staged kernel there; at N = 8 the state-staged ring leaves
+// room for too few consumer warps, and zero_adam_step_tma_grad_kernel below is
+// used instead).
 // One CTA per SM.  Warp 0 lane 0 is the producer: for each 2048-element tile
 // it issues one bulk copy (cp.async.bulk, the TMA engine) per rank's gradient
 // tile and per state array into a two-stage shared-memory ring, and the
@@ -490,6 +494,173 @@ bool launch_tma(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* err) {
   return true;
 }
 
+// ---------------------------------------------------------------------------
+// TMA-staged gradients, register-staged state: the variant for N = 8, bf16
+// gradients, fp32 sum.  One CTA per SM.  The producer lane bulk-copies only
+// the N gradient tiles of each 3072-element tile into a three-stage ring
+// (8 x 6 KB per stage).  Each of the 24 consumer warps' threads owns 4
+// elements of the tile: it loads their master, m and v straight into
+// registers before it waits for the stage, so those loads overlap the
+// gradient copies, then sums the gradients from shared memory, runs
+// adam_element and stores.  At N = 8 an element carries 42 bytes instead of
+// 58, so the arithmetic per byte is higher than at N = 16: with the state
+// staged too, only 8 consumer warps fit beside the ring and they fall behind
+// the copies; with the gradients alone, 24 do not.  Waits are bounded as in
+// the kernel above, with the same status word.
+
+constexpr int kTgEpt = 4;                          // elements per consumer thread
+constexpr int kTgConsumers = 768;                  // 24 warps
+constexpr int kTgTile = kTgConsumers * kTgEpt;     // 3072 elements
+constexpr int kTgStages = 3;
+
+constexpr size_t tma_grad_smem_bytes(int nt) {
+  return static_cast<size_t>(kTgStages) * nt * kTgTile * 2;
+}
+static_assert(tma_grad_smem_bytes(8) <= 227 * 1024, "ring exceeds one CTA's shared memory");
+
+template <int NT>
+__global__ void __launch_bounds__(kTgConsumers + 32, 1)
+    zero_adam_step_tma_grad_kernel(const __grid_constant__ TmaArgs<NT> a) {
+  constexpr int64_t kGradBytes = kTgTile * 2;  // one rank's gradient tile
+  constexpr int64_t kStage = NT * kGradBytes;
+  extern __shared__ __align__(1024) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kTgStages], empty[kTgStages];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t ntiles = (a.nbody + kTgTile - 1) / kTgTile;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTgStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kTgConsumers / 32);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane != 0) return;
+    int64_t k = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+      const int s = static_cast<int>(k % kTgStages);
+      if (k >= kTgStages &&
+          !mbar_wait(&empty[s], static_cast<uint32_t>((k / kTgStages - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const int64_t e0 = tile * kTgTile;
+      int64_t cnt = a.nbody - e0;
+      if (cnt > kTgTile) cnt = kTgTile;
+      const uint32_t gbytes = static_cast<uint32_t>(cnt * 2);  // a multiple of 16
+      uint8_t* st = ring + s * kStage;
+      mbar_expect_tx(&full[s], gbytes * NT);
+      for (int r = 0; r < NT; ++r) bulk_load(st + r * kGradBytes, a.g[r] + e0, gbytes, &full[s]);
+    }
+    if (!ok) {
+      atomicExch(&g_step_status, 1);
+      const int64_t first = k > kTgStages ? k - kTgStages : 0;
+      for (int64_t j = first; j < k; ++j)
+        mbar_wait(&full[j % kTgStages], static_cast<uint32_t>((j / kTgStages) & 1));
+    }
+    return;
+  }
+
+  const int t = threadIdx.x - 32;
+  int64_t k = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = static_cast<int>(k % kTgStages);
+    const int64_t e0 = tile * kTgTile + kTgEpt * t;
+    const bool in = e0 < a.nbody;  // e0 is a multiple of 4, nbody of 8: all 4 are in
+    float4 w = make_float4(0.f, 0.f, 0.f, 0.f), mm = w, vv = w;
+    if (in) {
+      w = ld_state(reinterpret_cast<const float4*>(a.master + e0));
+      mm = ld_state(reinterpret_cast<const float4*>(a.m + e0));
+      vv = ld_state(reinterpret_cast<const float4*>(a.v + e0));
+    }
+    if (!mbar_wait(&full[s], static_cast<uint32_t>((k / kTgStages) & 1))) {
+      atomicExch(&g_step_status, 2);
+      return;
+    }
+    const uint8_t* st = ring + s * kStage;
+    float acc[4] = {-0.0f, -0.0f, -0.0f, -0.0f};
+    if (in) {
+#pragma unroll
+      for (int r = 0; r < NT; ++r) {
+        const uint2 q = *reinterpret_cast<const uint2*>(st + r * kGradBytes + 2 * kTgEpt * t);
+        acc[0] = __fadd_rn(acc[0], bf16_lo(q.x));
+        acc[1] = __fadd_rn(acc[1], bf16_hi(q.x));
+        acc[2] = __fadd_rn(acc[2], bf16_lo(q.y));
+        acc[3] = __fadd_rn(acc[3], bf16_hi(q.y));
+      }
+    }
+    // every lane has read its slice of stage s: the warp hands the stage back
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (in) {
+      adam_element(acc[0], a.s, w.x, mm.x, vv.x);
+      adam_element(acc[1], a.s, w.y, mm.y, vv.y);
+      adam_element(acc[2], a.s, w.z, mm.z, vv.z);
+      adam_element(acc[3], a.s, w.w, mm.w, vv.w);
+      __stcs(reinterpret_cast<float4*>(a.master + e0), w);
+      __stcs(reinterpret_cast<float4*>(a.m + e0), mm);
+      __stcs(reinterpret_cast<float4*>(a.v + e0), vv);
+      __stcs(reinterpret_cast<uint2*>(a.param + e0),
+             make_uint2(pack_bf16x2_rn(w.x, w.y), pack_bf16x2_rn(w.z, w.w)));
+    }
+  }
+  // the last few (< 8) elements of the range, one per thread of block 0
+  if (blockIdx.x == 0 && a.nbody + t < a.n) {
+    const int64_t e = a.nbody + t;
+    float acc = -0.0f;
+#pragma unroll
+    for (int r = 0; r < NT; ++r) acc = __fadd_rn(acc, bf16_to_f32(ld_grad(a.g[r] + e)));
+    float w = ld_state(a.master + e), mm = ld_state(a.m + e), vv = ld_state(a.v + e);
+    adam_element(acc, a.s, w, mm, vv);
+    a.master[e] = w;
+    a.m[e] = mm;
+    a.v[e] = vv;
+    a.param[e] = f32_to_bf16_rn(w);
+  }
+}
+
+// As launch_tma, for the gradient-staged kernel.
+template <int NT>
+bool launch_tma_grad(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* err) {
+  if (!(a.head == 0 && a.gvec && a.svec && a.pvec) || a.nvec < 1) return false;
+  static std::mutex mu;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(zero_adam_step_tma_grad_kernel<NT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tma_grad_smem_bytes(NT))) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+      }
+      configured[dev] = true;
+    }
+  }
+  int sms = 0;
+  if (device_sm_count(&sms) != 0) return false;
+  TmaArgs<NT> t;
+  for (int k = 0; k < NT; ++k) t.g[k] = static_cast<const uint16_t*>(L.grads[k]);
+  t.master = L.master;
+  t.m = L.m;
+  t.v = L.v;
+  t.param = L.param;
+  t.n = L.n;
+  t.nbody = 8 * a.nvec;
+  t.s = L.s;
+  const int64_t ntiles = (t.nbody + kTgTile - 1) / kTgTile;
+  const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
+  zero_adam_step_tma_grad_kernel<NT>
+      <<<grid, kTgConsumers + 32, tma_grad_smem_bytes(NT), L.stream>>>(t);
+  *err = cudaGetLastError();
+  return true;
+}
+
 // Resident blocks per SM of a kernel on the current device (cached).
 int blocks_per_sm(const void* kernel) {
   static std::mutex mu;
@@ -557,6 +728,10 @@ cudaError_t launch_world(const StepLaunch& L) {
   if constexpr (NT == 16 && CAP == 16 && !GF32 && !ABF16) {
     cudaError_t err = cudaSuccess;
     if (launch_tma<16>(L, a, &err)) return err;
+  }
+  if constexpr (NT == 8 && CAP == 8 && !GF32 && !ABF16) {
+    cudaError_t err = cudaSuccess;
+    if (launch_tma_grad<8>(L, a, &err)) return err;
   }
 
   const void* kern = reinterpret_cast<const void*>(&zero_adam_step_kernel<NT, CAP, GF32, ABF16>);
