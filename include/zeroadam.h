@@ -21,6 +21,11 @@
  *     between calls is a per-device status word that a kernel sets only if one
  *     of its bounded waits gives up (see zero_device_status).  Faults inside a
  *     launched kernel surface, as for any CUDA work, at the caller's next sync.
+ *   - Tracing: zero_adam_step, zero_adam_step_range, zero3_unit_gather,
+ *     zero3_unit_gather_rows and zero_device_status each open an NVTX range
+ *     named after the function for the duration of the call (visible to
+ *     Nsight tools and any NVTX injection library; free when none is
+ *     attached).
  *   - Calls on different streams may run concurrently when their output
  *     buffers are disjoint; a sequence of calls may be captured into a CUDA
  *     graph after each kernel's first call on the device (which does one-time
@@ -236,14 +241,30 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
  * Device-side status of the library's kernels on the current device.  Some
  * launches stage data through shared memory with asynchronous bulk copies and
  * wait on hardware barriers; every such wait is bounded, and a wait that gives
- * up (seconds without progress) ends the launch early, leaving that step's
- * outputs incomplete, and records the fact in a per-device status word.
+ * up (one second without progress, by the GPU's global timer) ends the launch
+ * early, leaving that step's outputs incomplete, and records the fact in a
+ * per-device status word.
  * Returns ZERO_OK if no wait has given up since the previous call, else
  * ZERO_E_TIMEOUT; either way the word is cleared.  ZERO_E_DEVICE if there is no
  * usable device.  Unlike the other calls this one synchronises the current
  * device (it reads device memory).
  */
 int zero_device_status(void);
+
+/*
+ * Test hook for the bounded waits; the pages' method has no counterpart.
+ * While `on` is nonzero, every step launch that uses a TMA-staged kernel
+ * (world 8 or 16, bf16 gradients, fp32 sum, all buffers 16-byte aligned at
+ * the stepped range's first element) tells its producers to issue no copies.
+ * Every consumer's wait then runs out after its limit (about one second), no
+ * output of that step is written, and zero_device_status reports
+ * ZERO_E_TIMEOUT; the device and its context stay usable.  Launches of the
+ * other kernels are unaffected (they do not wait).  The setting is
+ * process-wide and read when a step is launched.  Returns the previous
+ * setting (0 or 1).  It exists so that tests can exercise the timeout path
+ * without faulting or hanging a GPU; production code never calls it.
+ */
+int zero_test_withhold_copies(int on);
 
 /* Text for a status code.  For ZERO_E_LAUNCH it includes the CUDA error text
    of this thread's last failed launch.  The pointer stays valid until this

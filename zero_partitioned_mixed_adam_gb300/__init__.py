@@ -33,7 +33,8 @@ ERRORS = {
 
 # Every symbol include/zeroadam.h declares.
 EXPORTS = ("zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero3_unit_gather_rows", "zero_device_status", "zero_strerror", "zero_version")
+           "zero3_unit_gather_rows", "zero_device_status", "zero_test_withhold_copies",
+           "zero_strerror", "zero_version")
 
 
 class ZeroError(RuntimeError):
@@ -83,6 +84,8 @@ def _load() -> ctypes.CDLL:
     lib.zero3_unit_gather_rows.restype = ctypes.c_int
     lib.zero_device_status.argtypes = []
     lib.zero_device_status.restype = ctypes.c_int
+    lib.zero_test_withhold_copies.argtypes = [ctypes.c_int]
+    lib.zero_test_withhold_copies.restype = ctypes.c_int
     lib.zero_strerror.argtypes = [ctypes.c_int]
     lib.zero_strerror.restype = ctypes.c_char_p
     lib.zero_version.argtypes = []
@@ -203,6 +206,13 @@ def device_status() -> int:
     return _lib.zero_device_status()
 
 
+def test_withhold_copies(on: bool) -> bool:
+    """Test hook: while on, the TMA-staged step kernels issue no copies, so their
+    bounded waits run out (zero_device_status then reports ZERO_E_TIMEOUT).
+    Returns the previous setting."""
+    return bool(_lib.zero_test_withhold_copies(1 if on else 0))
+
+
 def version() -> int:
     return _lib.zero_version()
 
@@ -213,7 +223,7 @@ def raw_lib() -> ctypes.CDLL:
 
 
 __all__ = ["zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero3_unit_gather_rows", "rows_layout", "device_status",
+           "zero3_unit_gather_rows", "rows_layout", "device_status", "test_withhold_copies",
            "ZeroPlan", "ZeroError", "strerror", "version", "raw_lib", "ZERO_ALL_RANKS",
            "ZERO_GRAD_FULL", "ZERO_GRAD_SHARD", "ZERO_GRAD_WINDOW", "ZERO_GRAD_F32",
            "ZERO_ACC_BF16", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "EXPORTS", "LIB_PATH"]

@@ -285,15 +285,15 @@ __global__ void __launch_bounds__(kThreads)
 // tile and per state array into a two-stage shared-memory ring, and the
 // stage's mbarrier completes when all bytes have landed.  Warps 1..8 consume:
 // each thread sums its 8 elements over the ranks and runs adam_element from
-// shared memory, then stores to global.  Every wait is bounded; a wait that
-// gives up records a nonzero status in g_step_status (read by
-// zero_device_status), the producer waits (bounded) for its own copies, and
-// every thread returns.
+// shared memory, then stores to global.  Every wait is bounded by about one
+// second of the GPU's global timer; a wait that gives up records a nonzero
+// status in g_step_status (read by zero_device_status), the producer waits
+// (bounded) for the copies it issued, and every thread returns.
 
 constexpr int kTmaTile = 2048;       // elements per tile
 constexpr int kTmaConsumers = 256;   // 8 warps, 8 elements per thread
 constexpr int kTmaStages = 2;
-constexpr uint32_t kTmaSpin = 1u << 22;  // try_wait polls before a wait gives up
+constexpr uint64_t kTmaWaitNs = 1000000000ull;  // a wait gives up after one second
 
 __device__ int g_step_status;
 
@@ -306,6 +306,7 @@ struct TmaArgs {
   uint16_t* param;
   int64_t n;      // elements in the range
   int64_t nbody;  // multiple of 8: [0, nbody) through the ring, [nbody, n) scalar
+  int32_t withhold;  // test hook: the producer issues no copies, so every wait runs out
   AdamScalars s;
 };
 
@@ -323,19 +324,29 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
 }
-// Bounded wait for the completion of the barrier phase of the given parity.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the completion of the barrier phase of the given parity; false if
+// it has not completed after kTmaWaitNs of the global timer.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
-  for (uint32_t i = 0; i < kTmaSpin; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_addr(b)), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(b, parity))
+    if (global_ns() - t0 > kTmaWaitNs) return false;
+  return true;
 }
 // 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.  Both
 // addresses 16-byte aligned, bytes a multiple of 16.
@@ -378,6 +389,7 @@ __global__ void __launch_bounds__(kTmaConsumers + 32, 1)
         ok = false;
         break;
       }
+      if (a.withhold) continue;
       const int64_t e0 = tile * kTmaTile;
       int64_t cnt = a.nbody - e0;
       if (cnt > kTmaTile) cnt = kTmaTile;
@@ -393,7 +405,7 @@ __global__ void __launch_bounds__(kTmaConsumers + 32, 1)
     if (!ok) {
       atomicExch(&g_step_status, 1);
       const int64_t first = k > kTmaStages ? k - kTmaStages : 0;
-      for (int64_t j = first; j < k; ++j)
+      for (int64_t j = first; j < k && !a.withhold; ++j)
         mbar_wait(&full[j % kTmaStages], static_cast<uint32_t>((j / kTmaStages) & 1));
     }
     return;
@@ -485,6 +497,7 @@ bool launch_tma(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* err) {
   t.param = L.param;
   t.n = L.n;
   t.nbody = 8 * a.nvec;
+  t.withhold = L.withhold;
   t.s = L.s;
   const int64_t ntiles = (t.nbody + kTmaTile - 1) / kTmaTile;
   const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
@@ -547,6 +560,7 @@ __global__ void __launch_bounds__(kTgConsumers + 32, 1)
         ok = false;
         break;
       }
+      if (a.withhold) continue;
       const int64_t e0 = tile * kTgTile;
       int64_t cnt = a.nbody - e0;
       if (cnt > kTgTile) cnt = kTgTile;
@@ -558,7 +572,7 @@ __global__ void __launch_bounds__(kTgConsumers + 32, 1)
     if (!ok) {
       atomicExch(&g_step_status, 1);
       const int64_t first = k > kTgStages ? k - kTgStages : 0;
-      for (int64_t j = first; j < k; ++j)
+      for (int64_t j = first; j < k && !a.withhold; ++j)
         mbar_wait(&full[j % kTgStages], static_cast<uint32_t>((j / kTgStages) & 1));
     }
     return;
@@ -652,6 +666,7 @@ bool launch_tma_grad(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* er
   t.param = L.param;
   t.n = L.n;
   t.nbody = 8 * a.nvec;
+  t.withhold = L.withhold;
   t.s = L.s;
   const int64_t ntiles = (t.nbody + kTgTile - 1) / kTgTile;
   const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);

@@ -1,7 +1,12 @@
 // capi.cpp -- the extern "C" entry points of libzeroadam.so (include/zeroadam.h):
 // argument checking, the shard planner, the fp32 scalars, kernel dispatch.
+// Every entry point that launches work, or waits for it, opens an NVTX range
+// named after itself for its whole duration (a no-op unless a profiler or
+// another NVTX tool is attached).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -37,6 +42,18 @@ int device_sm_count(int* sms) {
 }
 
 namespace {
+
+// Scoped NVTX range.
+struct Trace {
+  explicit Trace(const char* name) { nvtxRangePushA(name); }
+  ~Trace() { nvtxRangePop(); }
+  Trace(const Trace&) = delete;
+  Trace& operator=(const Trace&) = delete;
+};
+
+// zero_test_withhold_copies: read by every step launch (relaxed; a test sets it
+// between launches).
+std::atomic<int> g_withhold{0};
 
 thread_local cudaError_t t_last_cuda = cudaSuccess;
 thread_local std::string t_msg;
@@ -108,22 +125,11 @@ Range bytes_of(const void* p, int64_t first, int64_t count, int esize) {
   return {b, b + static_cast<uintptr_t>(count) * esize};
 }
 
-}  // namespace
-}  // namespace zeroadam
-
-using namespace zeroadam;
-
-extern "C" {
-
-int zero_plan(int64_t numel, int32_t world, zero_plan_t* out) {
-  if (out == nullptr) return ZERO_E_NULLPTR;
-  return make_plan(numel, world, out);
-}
-
-int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end,
-                         const void* const* grad_ptrs, int32_t grad_layout, float* master,
-                         float* m, float* v, void* param_bf16, int32_t param_layout, double lr,
-                         double beta1, double beta2, double eps, int64_t t, void* stream) {
+// The checks and the launch of one step over [begin, end) (both entry points).
+int step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end,
+               const void* const* grad_ptrs, int32_t grad_layout, float* master, float* m,
+               float* v, void* param_bf16, int32_t param_layout, double lr, double beta1,
+               double beta2, double eps, int64_t t, void* stream) {
   int rc = check_plan(plan);
   if (rc != ZERO_OK) return rc;
   const int32_t N = static_cast<int32_t>(plan->world);
@@ -205,6 +211,7 @@ int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, i
   L.param = static_cast<uint16_t*>(param_bf16) + p_first;
   L.n = n;
   L.stream = static_cast<cudaStream_t>(stream);
+  L.withhold = g_withhold.load(std::memory_order_relaxed);
   AdamScalars& s = L.s;
   s.b1 = static_cast<float>(beta1);
   s.omb1 = static_cast<float>(1.0 - beta1);
@@ -220,17 +227,42 @@ int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, i
   return launch_status(launch_adam_step(L));
 }
 
+}  // namespace
+}  // namespace zeroadam
+
+using namespace zeroadam;
+
+extern "C" {
+
+int zero_plan(int64_t numel, int32_t world, zero_plan_t* out) {
+  if (out == nullptr) return ZERO_E_NULLPTR;
+  return make_plan(numel, world, out);
+}
+
+int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end,
+                         const void* const* grad_ptrs, int32_t grad_layout, float* master,
+                         float* m, float* v, void* param_bf16, int32_t param_layout, double lr,
+                         double beta1, double beta2, double eps, int64_t t, void* stream) {
+  Trace trace("zero_adam_step_range");
+  return step_range(plan, rank, begin, end, grad_ptrs, grad_layout, master, m, v, param_bf16,
+                    param_layout, lr, beta1, beta2, eps, t, stream);
+}
+
 int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* grad_ptrs,
                    int32_t grad_layout, float* master, float* m, float* v, void* param_bf16,
                    int32_t param_layout, double lr, double beta1, double beta2, double eps,
                    int64_t t, void* stream) {
+  Trace trace("zero_adam_step");
   if ((grad_layout & ZERO_GRAD_LAYOUT_MASK) == ZERO_GRAD_WINDOW) return ZERO_E_LAYOUT;
-  return zero_adam_step_range(plan, rank, 0, INT64_MAX, grad_ptrs, grad_layout, master, m, v,
-                              param_bf16, param_layout, lr, beta1, beta2, eps, t, stream);
+  return step_range(plan, rank, 0, INT64_MAX, grad_ptrs, grad_layout, master, m, v, param_bf16,
+                    param_layout, lr, beta1, beta2, eps, t, stream);
 }
+
+int zero_test_withhold_copies(int on) { return g_withhold.exchange(on != 0 ? 1 : 0); }
 
 int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs,
                       void* full_bf16, void* stream) {
+  Trace trace("zero3_unit_gather");
   int rc = check_plan(unit_plan);
   if (rc != ZERO_OK) return rc;
   const int32_t N = static_cast<int32_t>(unit_plan->world);
@@ -259,6 +291,7 @@ int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptr
 int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t* cols,
                            int32_t world, const void* const* shard_ptrs, void* full_bf16,
                            void* stream) {
+  Trace trace("zero3_unit_gather_rows");
   if (ntensors < 1 || ntensors > ZERO_MAX_UNIT_TENSORS) return ZERO_E_SHAPE;
   if (world < 1 || world > ZERO_MAX_WORLD) return ZERO_E_WORLD;
   if (rows == nullptr || cols == nullptr || shard_ptrs == nullptr || full_bf16 == nullptr)
@@ -300,6 +333,7 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
 }
 
 int zero_device_status(void) {
+  Trace trace("zero_device_status");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_E_DEVICE;
   int word = 0;

@@ -35,6 +35,7 @@ struct StepLaunch {
   int64_t n;
   AdamScalars s;
   cudaStream_t stream;
+  int32_t withhold;  // test hook for the TMA-staged kernels (zero_test_withhold_copies)
 };
 
 // One launch of the ZeRO-3 unit gather.
