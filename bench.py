@@ -21,6 +21,7 @@ host cores on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -420,7 +421,9 @@ def run_ours(args, wl):
     if world_size > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        # a rank that dies fails the others' next collective after this, not after 30 min
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo",
+                                timeout=datetime.timedelta(minutes=10))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
