@@ -737,7 +737,8 @@ def run_zero2_buckets(args):
         "roofline": {"bound": "hbm", "achieved": nbytes / (t_buckets * 1e-3) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": nbytes / (t_buckets * 1e-3) / 1e9 / peak,
                      "traffic": None, "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-                     "kernel": "zero_adam_step_kernel (per bucket)",
+                     "kernel": "zero_adam_step_tma_grad_kernel (per bucket: N = 8, aligned "
+                               "bucket buffers and offsets)",
                      "algorithmic_bytes_per_launch": (2 * N + 26) * B,
                      "avg_launch_ms": t_buckets / len(starts)},
         "gpu_launches": len(starts) * (N + 1), "e2e": None, "cpu_baseline": None,
