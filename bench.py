@@ -184,8 +184,15 @@ class Replica:
         # (name, algorithmic bytes) of the step's launches, in order
         self.kernels = []
         if self.unit:
-            self.kernels.append(("zero3_unit_gather_kernel", 4 * wl.numel))
+            self.kernels.append((self.gather_kernel_name(), 4 * wl.numel))
         self.kernels.append((self.step_kernel_name(), _bytes_per_step(wl, plan)))
+
+    def gather_kernel_name(self):
+        """The library copies on the TMA engine when the shard is a multiple of 8
+        elements and every buffer is 16-byte aligned (whole cudaMalloc buffers)."""
+        tma = (self.wl.numel >= 8 and self.plan.shard % 8 == 0
+               and all(x.data_ptr() % 16 == 0 for x in self.shards + [self.full]))
+        return "zero3_unit_gather_tma_kernel" if tma else "zero3_unit_gather_kernel"
 
     def step_kernel_name(self):
         """The library runs a TMA-staged kernel for N = 16 (gradients and state
@@ -476,12 +483,16 @@ def run_ours(args, wl):
     dom = max(per_kernel, key=lambda k: k["avg_launch_ms"] * 1)
     peak, peak_src = _peaks()
     traffic = None
+    src, units = None, 0
     if dom["kernel"].startswith("zero_adam_step"):
-        rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc",
-                                           "adam_step.cu"))
+        src, units = "adam_step.cu", rep.n            # per stepped element
+    elif dom["kernel"].startswith("zero3_unit_gather"):
+        src, units = "unit_gather.cu", wl.numel       # per unit element
+    if src:
+        rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc", src))
         rec = (rec or {}).get(f"{dom['kernel']}/N{wl.world}")
         if rec:
-            traffic = rec["dram_bytes_per_element"] * rep.n
+            traffic = rec["dram_bytes_per_element"] * units
 
     e2e = None
     cpu = None

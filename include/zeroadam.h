@@ -208,6 +208,10 @@ int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, i
  *               unit_plan->shard elements each.
  *   full_bf16   device bf16 buffer of >= numel elements, written only; must not
  *               overlap a shard (ZERO_E_ALIAS).
+ *
+ * When shard is a multiple of 8 elements and every buffer is 16-byte aligned
+ * (whole cudaMalloc/PyTorch buffers) the copy runs on the TMA engine, whose
+ * waits are bounded (see zero_device_status); otherwise a load/store kernel.
  */
 int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs,
                       void* full_bf16, void* stream);
@@ -255,11 +259,12 @@ int zero_device_status(void);
  * Test hook for the bounded waits; the pages' method has no counterpart.
  * While `on` is nonzero, every step launch that uses a TMA-staged kernel
  * (world 8 or 16, bf16 gradients, fp32 sum, all buffers 16-byte aligned at
- * the stepped range's first element) tells its producers to issue no copies.
- * Every consumer's wait then runs out after its limit (about one second), no
- * output of that step is written, and zero_device_status reports
- * ZERO_E_TIMEOUT; the device and its context stay usable.  Launches of the
- * other kernels are unaffected (they do not wait).  The setting is
+ * the stepped range's first element) and every zero3_unit_gather that uses
+ * the TMA copy (shard a multiple of 8 elements, all buffers 16-byte aligned)
+ * tells its producers to issue no copies.  Every wait then runs out after its
+ * limit (about one second), no output of that call is written, and
+ * zero_device_status reports ZERO_E_TIMEOUT; the device and its context stay
+ * usable.  Launches of the other kernels are unaffected (they do not wait).  The setting is
  * process-wide and read when a step is launched.  Returns the previous
  * setting (0 or 1).  It exists so that tests can exercise the timeout path
  * without faulting or hanging a GPU; production code never calls it.

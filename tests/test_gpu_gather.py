@@ -41,8 +41,12 @@ def _shards_host(U, N, S):
     return [synth.fill_host(C.unit_shard_spec(U, N, r), 0, S, synth.OUT_BF16) for r in range(N)]
 
 
+# shard % 8 == 0 (with aligned buffers) takes the TMA copy: (4096, 2), (1 << 20, 64), and
+# ragged units with a tail of U mod 8 elements, (7995, 8) and (163_837, 5), and empty
+# trailing shards, (113, 16); the rest take the load/store kernel
 @pytest.mark.parametrize("U,N", [(1, 1), (1, 4), (7, 3), (8, 8), (100, 9), (1001, 3), (4096, 2),
-                                 (65537, 8), (100_000, 64), (123_457, 65), (1 << 20, 64)])
+                                 (65537, 8), (100_000, 64), (123_457, 65), (1 << 20, 64),
+                                 (7995, 8), (163_837, 5), (113, 16), (3 * 8192 * 152 + 8, 1)])
 def test_gather_small_whole_unit(U, N):
     plan, bases, shards = _shards_dev(U, N)
     fb = torch.full((U + 2 * GUARD,), CANARY16, dtype=torch.int16, device="cuda")
@@ -54,9 +58,12 @@ def test_gather_small_whole_unit(U, N):
     assert bool((fb[:GUARD] == CANARY16).all()) and bool((fb[GUARD + U:] == CANARY16).all())
 
 
-@pytest.mark.parametrize("off_src,off_dst", [(1, 0), (0, 1), (3, 5), (4, 4)])
+@pytest.mark.parametrize("off_src,off_dst", [(1, 0), (0, 1), (3, 5), (4, 4), (8, 8), (8, 0),
+                                             (0, 4)])
 def test_gather_misaligned(off_src, off_dst):
-    U, N = 50_001, 4
+    """shard = 12,504 (a multiple of 8): offsets of 8 elements keep 16-byte alignment
+    (TMA copy, with a 5-element tail); the others do not (load/store kernel)."""
+    U, N = 50_013, 4
     plan, bases, shards = _shards_dev(U, N, off=off_src)
     fb = torch.full((U + off_dst + GUARD,), CANARY16, dtype=torch.int16, device="cuda")
     full = fb[off_dst:off_dst + U]

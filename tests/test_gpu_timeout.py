@@ -1,9 +1,9 @@
-"""The TMA-staged step kernels' bounded waits, driven to run out without faulting or
-hanging the GPU: the library's test hook makes the producers issue no copies, so every
-consumer's wait on its stage gives up after its limit (one second of the GPU's global
-timer).  The launch must end, write nothing, and leave ZERO_E_TIMEOUT in the device
-status word; the word must clear on reading, and the next normal step on the same
-context must give the same bits as a step that never saw the hook."""
+"""The bounded waits of the TMA kernels (the staged step kernels and the unit gather's
+copy), driven to run out without faulting or hanging the GPU: the library's test hook
+makes the producers issue no copies, so every wait on a stage gives up after its limit
+(one second of the GPU's global timer).  The launch must end, write nothing, and leave
+ZERO_E_TIMEOUT in the device status word; the word must clear on reading, and the next
+normal call on the same context must give the same bits as one that never saw the hook."""
 import time
 
 import pytest
@@ -90,4 +90,29 @@ def test_hook_leaves_the_register_staged_kernel_alone():
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(_bits(x), _bits(y))
+    assert za.device_status() == za.ZERO_OK
+
+
+def test_withheld_gather_times_out_and_the_context_survives():
+    U, N = 1_048_573, 8          # shard 131,072: the TMA copy, with a 5-element tail
+    plan = za.zero_plan(U, N)
+    assert plan.shard % 8 == 0
+    shards = [torch.full((plan.shard,), k + 1, dtype=torch.int16, device="cuda") for k in range(N)]
+    full = torch.full((U,), -7, dtype=torch.int16, device="cuda")
+    torch.cuda.synchronize()
+    assert za.device_status() == za.ZERO_OK
+    prev = za.test_withhold_copies(True)
+    try:
+        t0 = time.perf_counter()
+        za.zero3_unit_gather(plan, shards, full)
+        torch.cuda.synchronize()
+        waited = time.perf_counter() - t0
+    finally:
+        za.test_withhold_copies(prev)
+    assert za.device_status() == E_TIMEOUT
+    assert 0.5 < waited < 60, waited
+    assert bool((full == -7).all()), "a withheld gather wrote the unit"
+    za.zero3_unit_gather(plan, shards, full)
+    torch.cuda.synchronize()
+    assert torch.equal(full, torch.cat(shards)[:U])
     assert za.device_status() == za.ZERO_OK

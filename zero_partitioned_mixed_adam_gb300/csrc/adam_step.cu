@@ -33,6 +33,7 @@
 #include <unordered_map>
 
 #include "internal.h"
+#include "tma_ops.h"
 
 namespace zeroadam {
 namespace {
@@ -293,7 +294,6 @@ __global__ void __launch_bounds__(kThreads)
 constexpr int kTmaTile = 2048;       // elements per tile
 constexpr int kTmaConsumers = 256;   // 8 warps, 8 elements per thread
 constexpr int kTmaStages = 2;
-constexpr uint64_t kTmaWaitNs = 1000000000ull;  // a wait gives up after one second
 
 __device__ int g_step_status;
 
@@ -310,55 +310,6 @@ struct TmaArgs {
   AdamScalars s;
 };
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait for the completion of the barrier phase of the given parity; false if
-// it has not completed after kTmaWaitNs of the global timer.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
-  if (mbar_try_wait(b, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(b, parity))
-    if (global_ns() - t0 > kTmaWaitNs) return false;
-  return true;
-}
-// 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.  Both
-// addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* b) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(b))
-      : "memory");
-}
-
 template <int NT>
 __global__ void __launch_bounds__(kTmaConsumers + 32, 1)
     zero_adam_step_tma_kernel(const __grid_constant__ TmaArgs<NT> a) {
@@ -374,7 +325,7 @@ __global__ void __launch_bounds__(kTmaConsumers + 32, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kTmaConsumers / 32);
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   __syncthreads();
 
@@ -545,7 +496,7 @@ __global__ void __launch_bounds__(kTgConsumers + 32, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kTgConsumers / 32);
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   __syncthreads();
 

@@ -285,6 +285,7 @@ int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptr
   L.numel = unit_plan->numel;
   L.shard = unit_plan->shard;
   L.stream = static_cast<cudaStream_t>(stream);
+  L.withhold = g_withhold.load(std::memory_order_relaxed);
   return launch_status(launch_unit_gather(L));
 }
 
@@ -336,9 +337,10 @@ int zero_device_status(void) {
   Trace trace("zero_device_status");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_E_DEVICE;
-  int word = 0;
-  if (read_and_clear_step_status(&word) != 0) return ZERO_E_DEVICE;
-  return word == 0 ? ZERO_OK : ZERO_E_TIMEOUT;
+  int step = 0, gather = 0;
+  if (read_and_clear_step_status(&step) != 0) return ZERO_E_DEVICE;
+  if (read_and_clear_gather_status(&gather) != 0) return ZERO_E_DEVICE;
+  return step == 0 && gather == 0 ? ZERO_OK : ZERO_E_TIMEOUT;
 }
 
 const char* zero_strerror(int status) {

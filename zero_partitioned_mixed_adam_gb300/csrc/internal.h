@@ -46,6 +46,7 @@ struct GatherLaunch {
   int64_t numel;
   int64_t shard;
   cudaStream_t stream;
+  int32_t withhold;  // test hook for the TMA gather kernel (zero_test_withhold_copies)
 };
 
 // One launch of the FSDP2-style (dim-0 row-sharded) unit gather.  Offsets are
@@ -71,6 +72,8 @@ cudaError_t launch_adam_step(const StepLaunch& L);
 // every wait completed); read and cleared.  Returns -1 if CUDA fails.
 int read_and_clear_step_status(int* status);
 cudaError_t launch_unit_gather(const GatherLaunch& L);
+// Status word of the TMA gather kernel's bounded waits; as above.
+int read_and_clear_gather_status(int* status);
 cudaError_t launch_unit_gather_rows(const GatherRowsLaunch& L);
 
 }  // namespace zeroadam

@@ -4,11 +4,15 @@
 // GPU's memory the gather is a copy of N bf16 shards into one unit buffer:
 //   full[r*shard + j] = shard_r[j],  r*shard + j < numel.
 // It moves 4 bytes per unit element (2 read, 2 written) and is bound by HBM
-// bandwidth, or for small units by launch latency.
+// bandwidth, or for small units by launch latency.  Two kernels: a copy on the
+// TMA engine (bulk loads into a shared-memory ring, bulk stores out of it) when
+// every shard boundary falls on a 16-byte boundary, and a vectorised
+// load/store copy for every other layout.
 #include <mutex>
 #include <unordered_map>
 
 #include "internal.h"
+#include "tma_ops.h"
 
 namespace zeroadam {
 namespace {
@@ -58,6 +62,139 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t j = done + tid; j < cnt; j += nthreads) dst[j] = __ldcs(src + j);
 }
 
+// ---------------------------------------------------------------------------
+// The gather on the TMA engine.  Requirements (checked by the launcher): the
+// unit buffer and every shard 16-byte aligned, shard a multiple of 8 elements.
+// Then the unit's first u8 = numel rounded down to 8 elements split into
+// 8192-element (16 KB) chunks whose pieces -- a chunk crosses at most a few
+// shard boundaries -- all start on 16-byte boundaries and are multiples of 16
+// bytes long.  One thread per CTA (one CTA per SM) moves its chunks (chunk
+// blockIdx.x + i * gridDim.x) through a 4-slot ring: a bulk load per piece
+// into a slot, completing on the slot's mbarrier, then one bulk store of the
+// slot to the unit.  Loads run 3 chunks ahead; a slot is reloaded once the
+// store that read it has finished reading.  The last numel - u8 (< 8)
+// elements are copied by plain threads of block 0.  Measured against the
+// load/store kernel on GB300: 3 % faster on units of 2^29 elements (0.988 of
+// the copy peak), 1.5x on 2^24 and 2.4x on 2^20 (latency-bound) units.
+//
+// Every wait is bounded by the global timer; a wait that gives up records a
+// nonzero status in g_gather_status (read with the step kernels' word by
+// zero_device_status), waits (bounded) for the loads already issued and for
+// its stores, and returns.
+
+constexpr int kChunk = 8192;  // elements per chunk
+constexpr int kSlots = 4;     // ring of 4 x 16 KB
+
+__device__ int g_gather_status;
+
+template <int CAP>
+struct GatherTmaArgs {
+  const uint16_t* src[CAP];
+  uint16_t* full;
+  int64_t numel;
+  int64_t u8;     // numel rounded down to a multiple of 8: [0, u8) moves by TMA
+  int64_t shard;  // a multiple of 8
+  int32_t withhold;  // test hook: issue no loads, so every wait runs out
+};
+
+template <int CAP>
+__global__ void __launch_bounds__(32, 1)
+    zero3_unit_gather_tma_kernel(const __grid_constant__ GatherTmaArgs<CAP> a) {
+  extern __shared__ __align__(1024) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kSlots];
+  const int lane = threadIdx.x;
+  if (blockIdx.x == 0 && a.u8 + lane < a.numel && !a.withhold) {
+    const int64_t e = a.u8 + lane;
+    const int64_t r = e / a.shard;
+    a.full[e] = a.src[r][e - r * a.shard];
+  }
+  if (lane != 0) return;
+  const int64_t nchunks = (a.u8 + kChunk - 1) / kChunk;
+  if (blockIdx.x >= nchunks) return;
+  for (int s = 0; s < kSlots; ++s) mbar_init(&full[s], 1);
+  mbar_init_fence();
+  const int64_t mine = (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  auto first = [&](int64_t i) { return (blockIdx.x + i * gridDim.x) * static_cast<int64_t>(kChunk); };
+  auto last = [&](int64_t e0) { return e0 + kChunk < a.u8 ? e0 + kChunk : a.u8; };
+  auto load = [&](int64_t i) {
+    if (a.withhold) return;
+    const int s = static_cast<int>(i % kSlots);
+    const int64_t e0 = first(i), e1 = last(e0);
+    mbar_expect_tx(&full[s], static_cast<uint32_t>((e1 - e0) * 2));
+    uint8_t* slot = ring + static_cast<int64_t>(s) * kChunk * 2;
+    for (int64_t e = e0; e < e1;) {  // one piece per shard the chunk touches
+      const int64_t r = e / a.shard;
+      const int64_t pe = (r + 1) * a.shard < e1 ? (r + 1) * a.shard : e1;
+      bulk_load(slot + (e - e0) * 2, a.src[r] + (e - r * a.shard),
+                static_cast<uint32_t>((pe - e) * 2), &full[s]);
+      e = pe;
+    }
+  };
+  int64_t loaded = mine < kSlots - 1 ? mine : kSlots - 1;
+  for (int64_t i = 0; i < loaded; ++i) load(i);
+  for (int64_t i = 0; i < mine; ++i) {
+    const int s = static_cast<int>(i % kSlots);
+    if (!mbar_wait(&full[s], static_cast<uint32_t>((i / kSlots) & 1))) {
+      atomicExch(&g_gather_status, 1);
+      for (int64_t j = i; j < loaded && !a.withhold; ++j)  // issued loads land first
+        mbar_wait(&full[j % kSlots], static_cast<uint32_t>((j / kSlots) & 1));
+      break;
+    }
+    fence_async_shared();
+    const int64_t e0 = first(i);
+    bulk_store(a.full + e0, ring + static_cast<int64_t>(s) * kChunk * 2,
+               static_cast<uint32_t>((last(e0) - e0) * 2));
+    bulk_commit();
+    if (i + kSlots - 1 < mine) {
+      bulk_wait_read<1>();  // the store of chunk i - 1 has read slot (i - 1) % kSlots
+      load(i + kSlots - 1);
+      ++loaded;
+    }
+  }
+  bulk_wait_all();
+}
+
+template <int CAP>
+bool launch_tma_cap(const GatherLaunch& L, cudaError_t* err) {
+  const int64_t u8 = L.numel & ~static_cast<int64_t>(7);
+  bool ok = u8 > 0 && L.shard % 8 == 0 && (reinterpret_cast<uintptr_t>(L.full) & 15u) == 0;
+  for (int k = 0; k < L.world && ok; ++k)
+    ok = (reinterpret_cast<uintptr_t>(L.shards[k]) & 15u) == 0;
+  if (!ok) return false;
+  constexpr size_t kSmem = static_cast<size_t>(kSlots) * kChunk * 2;
+  static std::mutex mu;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(zero3_unit_gather_tma_kernel<CAP>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmem)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+      }
+      configured[dev] = true;
+    }
+  }
+  int sms = 0;
+  if (device_sm_count(&sms) != 0) return false;
+  GatherTmaArgs<CAP> a;
+  for (int k = 0; k < L.world; ++k) a.src[k] = L.shards[k];
+  for (int k = L.world; k < CAP; ++k) a.src[k] = nullptr;
+  a.full = L.full;
+  a.numel = L.numel;
+  a.u8 = u8;
+  a.shard = L.shard;
+  a.withhold = L.withhold;
+  const int64_t nchunks = (u8 + kChunk - 1) / kChunk;
+  const int grid = static_cast<int>(nchunks < sms ? nchunks : sms);
+  zero3_unit_gather_tma_kernel<CAP><<<grid, 32, kSmem, L.stream>>>(a);
+  *err = cudaGetLastError();
+  return true;
+}
+
 int gather_blocks_per_sm(const void* kernel) {
   static std::mutex mu;
   static std::unordered_map<const void*, int> cache[64];
@@ -76,6 +213,8 @@ int gather_blocks_per_sm(const void* kernel) {
 
 template <int CAP>
 cudaError_t launch_cap(const GatherLaunch& L) {
+  cudaError_t err = cudaSuccess;
+  if (launch_tma_cap<CAP>(L, &err)) return err;
   GatherArgs<CAP> a;
   bool vec = (reinterpret_cast<uintptr_t>(L.full) % 16 == 0) && (L.world == 1 || L.shard % 8 == 0);
   for (int k = 0; k < L.world; ++k) {
@@ -204,6 +343,17 @@ cudaError_t launch_unit_gather_rows(const GatherRowsLaunch& L) {
   if (L.world <= 8) return launch_rows_cap<8>(L);
   if (L.world <= 64) return launch_rows_cap<64>(L);
   return launch_rows_cap<1024>(L);
+}
+
+int read_and_clear_gather_status(int* status) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gather_status, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_gather_status, &zero, sizeof(int)) != cudaSuccess) return -1;
+  }
+  *status = v;
+  return 0;
 }
 
 cudaError_t launch_unit_gather(const GatherLaunch& L) {
