@@ -845,6 +845,17 @@ def run_zero3_prefetch(args):
     t_pipe = timed(lambda: prefetch_pass(L, gather, compute, main_s, side))
     peak, peak_src = _peaks()
     g_gbs = 4 * U * L / (t_g * 1e-3) / 1e9
+    # the library copies on the TMA engine when every tensor offset and row block is a
+    # multiple of 8 elements and every buffer is 16-byte aligned (this layout, whole buffers)
+    o, ok = 0, True
+    for rows, cols in LLAMA_LAYER:
+        ok = ok and o % 8 == 0 and (-(-rows // N) * cols) % 8 == 0
+        o += rows * cols
+    ok = ok and all(x.data_ptr() % 16 == 0 for x in full + [t for layer in shards for t in layer])
+    kname = "zero3_unit_gather_rows_tma_kernel" if ok else "zero3_unit_gather_rows_kernel"
+    rec = (_traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc",
+                                        "unit_gather.cu")) or {}).get(f"{kname}/N{N}")
+    traffic = rec["dram_bytes_per_element"] * U if rec else None
     line = {
         "metric": METRIC, "value": L * U / (t_pipe * 1e-3) / 1e9, "unit": "Gelem/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_pipe,
@@ -859,9 +870,9 @@ def run_zero3_prefetch(args):
         "computes_only_ms": t_c,
         "hidden_fraction_of_shorter": (t_ser - t_pipe) / min(t_g, t_c),
         "roofline": {"bound": "hbm", "achieved": g_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": g_gbs / peak, "traffic": None,
+                     "frac": g_gbs / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-                     "kernel": "zero3_unit_gather_rows_kernel",
+                     "kernel": kname,
                      "algorithmic_bytes_per_launch": 4 * U, "avg_launch_ms": t_g / L},
         "gpu_launches": L, "e2e": None, "cpu_baseline": None,
     }

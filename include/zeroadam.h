@@ -234,6 +234,11 @@ int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptr
  * or the unit's element count overflows), ZERO_E_WORLD, ZERO_E_NULLPTR,
  * ZERO_E_ALIGN (odd pointer), ZERO_E_ALIAS (output overlaps a shard),
  * ZERO_E_LAUNCH.
+ *
+ * When every tensor's offset in the unit and every R_i*cols[i] is a multiple of
+ * 8 elements and every buffer is 16-byte aligned (e.g. a Llama layer's weights
+ * from whole cudaMalloc/PyTorch buffers) the copy runs on the TMA engine, whose
+ * waits are bounded (see zero_device_status); otherwise a load/store kernel.
  */
 int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t* cols,
                            int32_t world, const void* const* shard_ptrs, void* full_bf16,
@@ -259,9 +264,9 @@ int zero_device_status(void);
  * Test hook for the bounded waits; the pages' method has no counterpart.
  * While `on` is nonzero, every step launch that uses a TMA-staged kernel
  * (world 8 or 16, bf16 gradients, fp32 sum, all buffers 16-byte aligned at
- * the stepped range's first element) and every zero3_unit_gather that uses
- * the TMA copy (shard a multiple of 8 elements, all buffers 16-byte aligned)
- * tells its producers to issue no copies.  Every wait then runs out after its
+ * the stepped range's first element) and every zero3_unit_gather or
+ * zero3_unit_gather_rows that uses the TMA copy (see those calls) tells its
+ * producers to issue no copies.  Every wait then runs out after its
  * limit (about one second), no output of that call is written, and
  * zero_device_status reports ZERO_E_TIMEOUT; the device and its context stay
  * usable.  Launches of the other kernels are unaffected (they do not wait).  The setting is

@@ -155,10 +155,14 @@ LLAMA_LAYER = [(4096, 4096)] * 4 + [(11008, 4096), (11008, 4096), (4096, 11008),
                                      (4096, 1)]
 
 
+# Layouts whose tensor offsets and per-rank row blocks are multiples of 8 elements take the
+# TMA copy: [(64, 10)] x 8, the 256-column mix, and the last one (a short last run, an empty
+# one for (9, 8), and a 4-element tail for (37, 4)); the others the load/store kernel.
 @pytest.mark.parametrize("shapes,world", [
     ([(10, 3)], 4), ([(7, 5), (1, 9), (13, 1)], 3), ([(3, 2)], 8), ([(64, 10)], 8),
     ([(1000, 17), (999, 33), (5, 1)], 16), ([(300, 7)] * 20, 64), ([(257, 129)], 65),
     ([(4096, 256), (11008, 256), (256, 1)], 8),
+    ([(1001, 8), (77, 16), (9, 8), (37, 4)], 4),
 ])
 def test_gather_rows_vs_oracle(shapes, world):
     host, dev, total = _rows_problem(shapes, world, seed=len(shapes) * 100 + world)

@@ -116,3 +116,33 @@ def test_withheld_gather_times_out_and_the_context_survives():
     torch.cuda.synchronize()
     assert torch.equal(full, torch.cat(shards)[:U])
     assert za.device_status() == za.ZERO_OK
+
+
+def test_withheld_row_gather_times_out_and_the_context_survives():
+    shapes, world = [(1001, 8), (77, 16), (9, 8), (37, 4)], 4   # the TMA row copy
+    shard_len, total = za.rows_layout(shapes, world)
+    shards = [torch.full((shard_len,), k + 1, dtype=torch.int16, device="cuda")
+              for k in range(world)]
+    full = torch.full((total,), -7, dtype=torch.int16, device="cuda")
+    torch.cuda.synchronize()
+    assert za.device_status() == za.ZERO_OK
+    prev = za.test_withhold_copies(True)
+    try:
+        za.zero3_unit_gather_rows(shapes, world, shards, full)
+        torch.cuda.synchronize()
+    finally:
+        za.test_withhold_copies(prev)
+    assert za.device_status() == E_TIMEOUT
+    assert bool((full == -7).all()), "a withheld row gather wrote the unit"
+    za.zero3_unit_gather_rows(shapes, world, shards, full)
+    torch.cuda.synchronize()
+    assert za.device_status() == za.ZERO_OK
+    # every element of tensor i's rows [r*R, (r+1)*R) comes from rank r
+    off = 0
+    for rows, cols in shapes:
+        R = -(-rows // world)
+        t = full[off:off + rows * cols].view(rows, cols)
+        for r in range(world):
+            blk = t[r * R:min((r + 1) * R, rows)]
+            assert bool((blk == r + 1).all())
+        off += rows * cols

@@ -330,6 +330,7 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
   L.shard_off = shard_off;
   L.full = static_cast<uint16_t*>(full_bf16);
   L.stream = static_cast<cudaStream_t>(stream);
+  L.withhold = g_withhold.load(std::memory_order_relaxed);
   return launch_status(launch_unit_gather_rows(L));
 }
 

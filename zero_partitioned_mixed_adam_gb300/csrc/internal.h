@@ -62,6 +62,7 @@ struct GatherRowsLaunch {
   const int64_t* shard_off;
   uint16_t* full;
   cudaStream_t stream;
+  int32_t withhold;  // test hook for the TMA row gather kernel (zero_test_withhold_copies)
 };
 
 // Streaming-multiprocessor count of the current device (cached per device).

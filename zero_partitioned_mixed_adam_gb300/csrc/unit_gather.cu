@@ -63,87 +63,56 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------------------------
-// The gather on the TMA engine.  Requirements (checked by the launcher): the
-// unit buffer and every shard 16-byte aligned, shard a multiple of 8 elements.
-// Then the unit's first u8 = numel rounded down to 8 elements split into
-// 8192-element (16 KB) chunks whose pieces -- a chunk crosses at most a few
-// shard boundaries -- all start on 16-byte boundaries and are multiples of 16
-// bytes long.  One thread per CTA (one CTA per SM) moves its chunks (chunk
-// blockIdx.x + i * gridDim.x) through a 4-slot ring: a bulk load per piece
-// into a slot, completing on the slot's mbarrier, then one bulk store of the
-// slot to the unit.  Loads run 3 chunks ahead; a slot is reloaded once the
-// store that read it has finished reading.  The last numel - u8 (< 8)
-// elements are copied by plain threads of block 0.  Measured against the
-// load/store kernel on GB300: 3 % faster on units of 2^29 elements (0.988 of
-// the copy peak), 1.5x on 2^24 and 2.4x on 2^20 (latency-bound) units.
+// The gathers on the TMA engine.  A copy is cut into chunks of up to 8192
+// elements (16 KB) whose pieces all start on 16-byte boundaries and are
+// multiples of 16 bytes long; the launchers check the layouts that guarantee
+// it.  One thread per CTA (one CTA per SM) moves its chunks (chunk
+// blockIdx.x + i * gridDim.x) through a 4-slot ring in shared memory: bulk
+// loads of a chunk's pieces into a slot, completing on the slot's mbarrier,
+// then one bulk store of the slot, committed as a bulk async-group.  Loads run
+// 3 chunks ahead; a slot is reloaded once the store that read it has finished
+// reading.  Elements that do not fill a 16-byte unit at the end of a run are
+// copied with plain loads and stores.  Measured against the load/store kernel
+// on GB300 (flat gather): the same bytes and time under ncu, 1-3 % faster back
+// to back on units of 202M and 2^29 elements (0.93-0.98 of the copy peak),
+// 1.5x on 2^24 and 2.4x on 2^20 units with the L2 warm.
 //
 // Every wait is bounded by the global timer; a wait that gives up records a
 // nonzero status in g_gather_status (read with the step kernels' word by
 // zero_device_status), waits (bounded) for the loads already issued and for
-// its stores, and returns.
+// its stores, and stops.
 
 constexpr int kChunk = 8192;  // elements per chunk
 constexpr int kSlots = 4;     // ring of 4 x 16 KB
+constexpr int64_t kSlotBytes = static_cast<int64_t>(kChunk) * 2;
+constexpr size_t kRingBytes = static_cast<size_t>(kSlots) * kSlotBytes;
 
 __device__ int g_gather_status;
 
-template <int CAP>
-struct GatherTmaArgs {
-  const uint16_t* src[CAP];
-  uint16_t* full;
-  int64_t numel;
-  int64_t u8;     // numel rounded down to a multiple of 8: [0, u8) moves by TMA
-  int64_t shard;  // a multiple of 8
-  int32_t withhold;  // test hook: issue no loads, so every wait runs out
-};
-
-template <int CAP>
-__global__ void __launch_bounds__(32, 1)
-    zero3_unit_gather_tma_kernel(const __grid_constant__ GatherTmaArgs<CAP> a) {
-  extern __shared__ __align__(1024) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[kSlots];
-  const int lane = threadIdx.x;
-  if (blockIdx.x == 0 && a.u8 + lane < a.numel && !a.withhold) {
-    const int64_t e = a.u8 + lane;
-    const int64_t r = e / a.shard;
-    a.full[e] = a.src[r][e - r * a.shard];
-  }
-  if (lane != 0) return;
-  const int64_t nchunks = (a.u8 + kChunk - 1) / kChunk;
-  if (blockIdx.x >= nchunks) return;
-  for (int s = 0; s < kSlots; ++s) mbar_init(&full[s], 1);
-  mbar_init_fence();
-  const int64_t mine = (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
-  auto first = [&](int64_t i) { return (blockIdx.x + i * gridDim.x) * static_cast<int64_t>(kChunk); };
-  auto last = [&](int64_t e0) { return e0 + kChunk < a.u8 ? e0 + kChunk : a.u8; };
+// One thread moves its CTA's `mine` chunks (chunk i of the CTA is chunk
+// blockIdx.x + i * gridDim.x of the copy) through the ring.  layout.load(i,
+// slot, bar) issues the bulk loads of the CTA's chunk i into `slot` and arms
+// `bar` with their byte count (zero bytes: the arrive alone completes the
+// phase); it is called for i = 0, 1, 2, ... in order.  layout.store(i, slot)
+// issues chunk i's bulk store, if it has any bytes.
+template <class Layout>
+__device__ void ring_copy(Layout& layout, int64_t mine, uint8_t* ring, uint64_t* bar,
+                          bool withhold) {
   auto load = [&](int64_t i) {
-    if (a.withhold) return;
-    const int s = static_cast<int>(i % kSlots);
-    const int64_t e0 = first(i), e1 = last(e0);
-    mbar_expect_tx(&full[s], static_cast<uint32_t>((e1 - e0) * 2));
-    uint8_t* slot = ring + static_cast<int64_t>(s) * kChunk * 2;
-    for (int64_t e = e0; e < e1;) {  // one piece per shard the chunk touches
-      const int64_t r = e / a.shard;
-      const int64_t pe = (r + 1) * a.shard < e1 ? (r + 1) * a.shard : e1;
-      bulk_load(slot + (e - e0) * 2, a.src[r] + (e - r * a.shard),
-                static_cast<uint32_t>((pe - e) * 2), &full[s]);
-      e = pe;
-    }
+    if (!withhold) layout.load(i, ring + (i % kSlots) * kSlotBytes, &bar[i % kSlots]);
   };
   int64_t loaded = mine < kSlots - 1 ? mine : kSlots - 1;
   for (int64_t i = 0; i < loaded; ++i) load(i);
   for (int64_t i = 0; i < mine; ++i) {
     const int s = static_cast<int>(i % kSlots);
-    if (!mbar_wait(&full[s], static_cast<uint32_t>((i / kSlots) & 1))) {
+    if (!mbar_wait(&bar[s], static_cast<uint32_t>((i / kSlots) & 1))) {
       atomicExch(&g_gather_status, 1);
-      for (int64_t j = i; j < loaded && !a.withhold; ++j)  // issued loads land first
-        mbar_wait(&full[j % kSlots], static_cast<uint32_t>((j / kSlots) & 1));
+      for (int64_t j = i; j < loaded && !withhold; ++j)  // issued loads land first
+        mbar_wait(&bar[j % kSlots], static_cast<uint32_t>((j / kSlots) & 1));
       break;
     }
     fence_async_shared();
-    const int64_t e0 = first(i);
-    bulk_store(a.full + e0, ring + static_cast<int64_t>(s) * kChunk * 2,
-               static_cast<uint32_t>((last(e0) - e0) * 2));
+    layout.store(i, ring + s * kSlotBytes);
     bulk_commit();
     if (i + kSlots - 1 < mine) {
       bulk_wait_read<1>();  // the store of chunk i - 1 has read slot (i - 1) % kSlots
@@ -154,6 +123,66 @@ __global__ void __launch_bounds__(32, 1)
   bulk_wait_all();
 }
 
+// Flat gather: shard a multiple of 8 elements, every buffer 16-byte aligned.
+// The unit's first u8 = numel rounded down to 8 elements is chunked; a chunk
+// is one piece per shard it touches.
+template <int CAP>
+struct GatherTmaArgs {
+  const uint16_t* src[CAP];
+  uint16_t* full;
+  int64_t numel;
+  int64_t u8;     // numel rounded down to a multiple of 8: [0, u8) moves by TMA
+  int64_t shard;  // a multiple of 8
+  int32_t withhold;  // test hook: issue no loads, so every wait runs out
+};
+
+// The CTA's chunk i covers [e0, e1): e0 = (blockIdx.x + i * gridDim.x) * kChunk.
+template <int CAP>
+struct FlatLayout {
+  const GatherTmaArgs<CAP>& a;
+  __device__ void range(int64_t i, int64_t* e0, int64_t* e1) const {
+    *e0 = (blockIdx.x + i * static_cast<int64_t>(gridDim.x)) * kChunk;
+    *e1 = *e0 + kChunk < a.u8 ? *e0 + kChunk : a.u8;
+  }
+  __device__ void load(int64_t i, uint8_t* slot, uint64_t* bar) const {
+    int64_t e0, e1;
+    range(i, &e0, &e1);
+    mbar_expect_tx(bar, static_cast<uint32_t>((e1 - e0) * 2));
+    for (int64_t e = e0; e < e1;) {  // one piece per shard the chunk touches
+      const int64_t r = e / a.shard;
+      const int64_t pe = (r + 1) * a.shard < e1 ? (r + 1) * a.shard : e1;
+      bulk_load(slot + (e - e0) * 2, a.src[r] + (e - r * a.shard),
+                static_cast<uint32_t>((pe - e) * 2), bar);
+      e = pe;
+    }
+  }
+  __device__ void store(int64_t i, const uint8_t* slot) const {
+    int64_t e0, e1;
+    range(i, &e0, &e1);
+    bulk_store(a.full + e0, slot, static_cast<uint32_t>((e1 - e0) * 2));
+  }
+};
+
+template <int CAP>
+__global__ void __launch_bounds__(32, 1)
+    zero3_unit_gather_tma_kernel(const __grid_constant__ GatherTmaArgs<CAP> a) {
+  extern __shared__ __align__(1024) uint8_t ring[];
+  __shared__ __align__(8) uint64_t bar[kSlots];
+  const int lane = threadIdx.x;
+  if (blockIdx.x == 0 && a.u8 + lane < a.numel && !a.withhold) {  // the last < 8 elements
+    const int64_t e = a.u8 + lane;
+    const int64_t r = e / a.shard;
+    a.full[e] = a.src[r][e - r * a.shard];
+  }
+  const int64_t nchunks = (a.u8 + kChunk - 1) / kChunk;
+  if (lane != 0 || blockIdx.x >= nchunks) return;
+  for (int s = 0; s < kSlots; ++s) mbar_init(&bar[s], 1);
+  mbar_init_fence();
+  const int64_t mine = (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  FlatLayout<CAP> layout{a};
+  ring_copy(layout, mine, ring, bar, a.withhold != 0);
+}
+
 template <int CAP>
 bool launch_tma_cap(const GatherLaunch& L, cudaError_t* err) {
   const int64_t u8 = L.numel & ~static_cast<int64_t>(7);
@@ -161,7 +190,6 @@ bool launch_tma_cap(const GatherLaunch& L, cudaError_t* err) {
   for (int k = 0; k < L.world && ok; ++k)
     ok = (reinterpret_cast<uintptr_t>(L.shards[k]) & 15u) == 0;
   if (!ok) return false;
-  constexpr size_t kSmem = static_cast<size_t>(kSlots) * kChunk * 2;
   static std::mutex mu;
   static bool configured[64] = {false};
   int dev = 0;
@@ -171,7 +199,7 @@ bool launch_tma_cap(const GatherLaunch& L, cudaError_t* err) {
     if (!configured[dev]) {
       if (cudaFuncSetAttribute(zero3_unit_gather_tma_kernel<CAP>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSmem)) != cudaSuccess) {
+                               static_cast<int>(kRingBytes)) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
       }
@@ -190,7 +218,7 @@ bool launch_tma_cap(const GatherLaunch& L, cudaError_t* err) {
   a.withhold = L.withhold;
   const int64_t nchunks = (u8 + kChunk - 1) / kChunk;
   const int grid = static_cast<int>(nchunks < sms ? nchunks : sms);
-  zero3_unit_gather_tma_kernel<CAP><<<grid, 32, kSmem, L.stream>>>(a);
+  zero3_unit_gather_tma_kernel<CAP><<<grid, 32, kRingBytes, L.stream>>>(a);
   *err = cudaGetLastError();
   return true;
 }
@@ -264,6 +292,23 @@ struct GatherRowsArgs {
 };
 
 template <int CAP>
+void fill_rows_args(const GatherRowsLaunch& L, GatherRowsArgs<CAP>* a) {
+  for (int k = 0; k < L.world; ++k) a->src[k] = L.shards[k];
+  for (int k = L.world; k < CAP; ++k) a->src[k] = nullptr;
+  a->full = L.full;
+  a->world = L.world;
+  a->ntensors = L.ntensors;
+  for (int i = 0; i < kMaxTensors; ++i) {
+    const bool in = i < L.ntensors;
+    a->rows[i] = in ? L.rows[i] : 0;
+    a->cols[i] = in ? L.cols[i] : 0;
+    a->per_rank[i] = in ? L.rows_per_rank[i] : 0;
+    a->full_off[i] = in ? L.full_off[i] : 0;
+    a->shard_off[i] = in ? L.shard_off[i] : 0;
+  }
+}
+
+template <int CAP>
 __global__ void __launch_bounds__(kThreads, 4)
     zero3_unit_gather_rows_kernel(const __grid_constant__ GatherRowsArgs<CAP> a) {
   const int64_t nseg = static_cast<int64_t>(a.ntensors) * a.world;
@@ -299,26 +344,171 @@ __global__ void __launch_bounds__(kThreads, 4)
   }
 }
 
+// Row gather on the TMA engine: every row block (tensor i, rank r) is a run of
+// nrows * cols elements at shard_off[i] in shard r and at
+// full_off[i] + r * per_rank[i] * cols[i] in the unit.  With full_off[i] and
+// per_rank[i] * cols[i] multiples of 8 (so shard_off[i] too) and every buffer
+// 16-byte aligned, each run starts on a 16-byte boundary at both ends.  Every
+// run of tensor i gets cps[i] = ceil(per_rank[i] * cols[i] / kChunk) chunk
+// numbers (the short or empty runs of the last ranks leave some of theirs
+// empty); chunk j belongs to the tensor i with prefix[i] <= j < prefix[i + 1].
+template <int CAP>
+struct RowsTmaArgs {
+  GatherRowsArgs<CAP> g;
+  int64_t cps[kMaxTensors];
+  int64_t prefix[kMaxTensors + 1];
+  int32_t withhold;  // test hook: issue no loads, so every wait runs out
+};
+
+// The CTA's chunks j = blockIdx.x + i * gridDim.x, walked as (tensor t, chunk k
+// within the tensor's world * cps[t] chunks); tables in shared memory.
+struct RowsTables {
+  int64_t rows[kMaxTensors], cols[kMaxTensors], per_rank[kMaxTensors];
+  int64_t full_off[kMaxTensors], shard_off[kMaxTensors], cps[kMaxTensors];
+};
+
+// Where a chunk held in a ring slot goes: one bulk store of `bytes` to `dst`.
+struct Pending {
+  uint16_t* dst;
+  uint32_t bytes;
+};
+
+struct RowsLayout {
+  const RowsTables& tb;
+  const uint16_t* const* src;
+  uint16_t* full;
+  Pending* pending;  // per ring slot, filled when the chunk is loaded
+  int32_t world, ntensors;
+  int64_t t, k, stride;
+  __device__ void skip() {  // move (t, k) past tensors whose chunks are used up
+    while (t < ntensors && k >= world * tb.cps[t]) {
+      k -= world * tb.cps[t];
+      ++t;
+    }
+  }
+  // chunk i is the next one of the walk: loads are issued in order
+  __device__ void load(int64_t i, uint8_t* slot, uint64_t* bar) {
+    const int64_t r = k / tb.cps[t];
+    const int64_t e0 = (k - r * tb.cps[t]) * kChunk;
+    const int64_t r0 = r * tb.per_rank[t];
+    int64_t nrows = tb.rows[t] - r0;
+    if (nrows > tb.per_rank[t]) nrows = tb.per_rank[t];
+    if (nrows < 0) nrows = 0;
+    const int64_t aligned = (nrows * tb.cols[t]) & ~static_cast<int64_t>(7);
+    int64_t e1 = e0 + kChunk < aligned ? e0 + kChunk : aligned;
+    if (e1 < e0) e1 = e0;
+    const uint32_t bytes = static_cast<uint32_t>((e1 - e0) * 2);
+    mbar_expect_tx(bar, bytes);
+    if (bytes) bulk_load(slot, src[r] + tb.shard_off[t] + e0, bytes, bar);
+    pending[i % kSlots] = Pending{full + tb.full_off[t] + r0 * tb.cols[t] + e0, bytes};
+    k += stride;
+    skip();
+  }
+  __device__ void store(int64_t i, const uint8_t* slot) const {
+    const Pending& p = pending[i % kSlots];
+    if (p.bytes) bulk_store(p.dst, slot, p.bytes);
+  }
+};
+
+template <int CAP>
+__global__ void __launch_bounds__(32, 1)
+    zero3_unit_gather_rows_tma_kernel(const __grid_constant__ RowsTmaArgs<CAP> a) {
+  extern __shared__ __align__(1024) uint8_t ring[];
+  __shared__ __align__(8) uint64_t bar[kSlots];
+  __shared__ Pending pending[kSlots];
+  __shared__ RowsTables tb;
+  __shared__ const uint16_t* src[CAP];
+  const GatherRowsArgs<CAP>& g = a.g;
+  const int lane = threadIdx.x;
+  // the last (< 8) elements of every run, all lanes of all CTAs
+  const int64_t nseg = static_cast<int64_t>(g.ntensors) * g.world;
+  for (int64_t seg = static_cast<int64_t>(blockIdx.x) * 32 + lane; seg < nseg && !a.withhold;
+       seg += static_cast<int64_t>(gridDim.x) * 32) {
+    const int i = static_cast<int>(seg / g.world);
+    const int64_t r = seg - static_cast<int64_t>(i) * g.world;
+    const int64_t r0 = r * g.per_rank[i];
+    int64_t nrows = g.rows[i] - r0;
+    if (nrows > g.per_rank[i]) nrows = g.per_rank[i];
+    if (nrows <= 0) continue;
+    const int64_t len = nrows * g.cols[i];
+    for (int64_t e = len & ~static_cast<int64_t>(7); e < len; ++e)
+      g.full[g.full_off[i] + r0 * g.cols[i] + e] = g.src[r][g.shard_off[i] + e];
+  }
+  const int64_t nchunks = a.prefix[g.ntensors];
+  if (blockIdx.x >= nchunks) return;
+  for (int i = lane; i < g.ntensors; i += 32) {
+    tb.rows[i] = g.rows[i];
+    tb.cols[i] = g.cols[i];
+    tb.per_rank[i] = g.per_rank[i];
+    tb.full_off[i] = g.full_off[i];
+    tb.shard_off[i] = g.shard_off[i];
+    tb.cps[i] = a.cps[i];
+  }
+  for (int k = lane; k < g.world; k += 32) src[k] = g.src[k];
+  __syncwarp();
+  if (lane != 0) return;
+  for (int s = 0; s < kSlots; ++s) mbar_init(&bar[s], 1);
+  mbar_init_fence();
+  const int64_t mine = (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  RowsLayout layout{tb, src, g.full, pending, g.world, g.ntensors, 0, blockIdx.x, gridDim.x};
+  layout.skip();
+  ring_copy(layout, mine, ring, bar, a.withhold != 0);
+}
+
+template <int CAP>
+bool launch_rows_tma(const GatherRowsLaunch& L, cudaError_t* err) {
+  bool ok = (reinterpret_cast<uintptr_t>(L.full) & 15u) == 0;
+  for (int k = 0; k < L.world && ok; ++k)
+    ok = (reinterpret_cast<uintptr_t>(L.shards[k]) & 15u) == 0;
+  for (int i = 0; i < L.ntensors && ok; ++i)
+    ok = L.full_off[i] % 8 == 0 && L.shard_off[i] % 8 == 0 &&
+         (L.rows_per_rank[i] * L.cols[i]) % 8 == 0;
+  if (!ok) return false;
+  static std::mutex mu;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(zero3_unit_gather_rows_tma_kernel<CAP>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kRingBytes)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+      }
+      configured[dev] = true;
+    }
+  }
+  int sms = 0;
+  if (device_sm_count(&sms) != 0) return false;
+  RowsTmaArgs<CAP> a;
+  fill_rows_args(L, &a.g);
+  a.prefix[0] = 0;
+  for (int i = 0; i < kMaxTensors; ++i) {
+    a.cps[i] = i < L.ntensors ? (L.rows_per_rank[i] * L.cols[i] + kChunk - 1) / kChunk : 0;
+    if (i < L.ntensors) a.prefix[i + 1] = a.prefix[i] + L.world * a.cps[i];
+    else a.prefix[i + 1] = a.prefix[i];
+  }
+  a.withhold = L.withhold;
+  const int64_t nchunks = a.prefix[L.ntensors];
+  const int grid = static_cast<int>(nchunks < sms ? nchunks : sms);
+  zero3_unit_gather_rows_tma_kernel<CAP><<<grid, 32, kRingBytes, L.stream>>>(a);
+  *err = cudaGetLastError();
+  return true;
+}
+
 template <int CAP>
 cudaError_t launch_rows_cap(const GatherRowsLaunch& L) {
+  cudaError_t err = cudaSuccess;
+  if (launch_rows_tma<CAP>(L, &err)) return err;
   GatherRowsArgs<CAP> a;
-  for (int k = 0; k < L.world; ++k) a.src[k] = L.shards[k];
-  for (int k = L.world; k < CAP; ++k) a.src[k] = nullptr;
-  a.full = L.full;
-  a.world = L.world;
-  a.ntensors = L.ntensors;
+  fill_rows_args(L, &a);
   int64_t biggest = 1;
   for (int i = 0; i < L.ntensors; ++i) {
-    a.rows[i] = L.rows[i];
-    a.cols[i] = L.cols[i];
-    a.per_rank[i] = L.rows_per_rank[i];
-    a.full_off[i] = L.full_off[i];
-    a.shard_off[i] = L.shard_off[i];
     const int64_t blk = L.rows_per_rank[i] * L.cols[i];
     if (blk > biggest) biggest = blk;
   }
-  for (int i = L.ntensors; i < kMaxTensors; ++i)
-    a.rows[i] = a.cols[i] = a.per_rank[i] = a.full_off[i] = a.shard_off[i] = 0;
 
   const void* kern = reinterpret_cast<const void*>(&zero3_unit_gather_rows_kernel<CAP>);
   int sms = 0;
