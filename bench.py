@@ -130,16 +130,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def code_hash(path):
+    """SHA-256 of a C++/CUDA source with its // comments, trailing blanks and empty
+    lines removed: it changes when the code does, not when a comment does."""
+    lines = []
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def _traffic_record(kernel_src):
     """DRAM traffic per element from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+    the current code of the kernel's source file (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        with open(kernel_src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        return rec.get(sha)
+        return rec.get(code_hash(kernel_src))
     except Exception:
         return None
 

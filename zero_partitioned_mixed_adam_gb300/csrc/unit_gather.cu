@@ -3,11 +3,12 @@
 // all-gathered from the ranks' shards).  With the ranks emulated in one
 // GPU's memory the gather is a copy of N bf16 shards into one unit buffer:
 //   full[r*shard + j] = shard_r[j],  r*shard + j < numel.
-// It moves 4 bytes per unit element (2 read, 2 written) and is bound by HBM
-// bandwidth, or for small units by launch latency.  Two kernels: a copy on the
-// TMA engine (bulk loads into a shared-memory ring, bulk stores out of it) when
-// every shard boundary falls on a 16-byte boundary, and a vectorised
-// load/store copy for every other layout.
+// The FSDP2-style gather (row blocks of each tensor per rank) is the same copy
+// in T*N runs.  Both move 4 bytes per unit element (2 read, 2 written) and are
+// bound by HBM bandwidth, or for small units by launch latency.  Each has two
+// kernels: a copy on the TMA engine (bulk loads into a shared-memory ring,
+// bulk stores out of it) when every run starts on a 16-byte boundary, and a
+// vectorised load/store copy for every other layout.
 #include <mutex>
 #include <unordered_map>
 
@@ -72,10 +73,11 @@ __global__ void __launch_bounds__(kThreads)
 // then one bulk store of the slot, committed as a bulk async-group.  Loads run
 // 3 chunks ahead; a slot is reloaded once the store that read it has finished
 // reading.  Elements that do not fill a 16-byte unit at the end of a run are
-// copied with plain loads and stores.  Measured against the load/store kernel
-// on GB300 (flat gather): the same bytes and time under ncu, 1-3 % faster back
-// to back on units of 202M and 2^29 elements (0.93-0.98 of the copy peak),
-// 1.5x on 2^24 and 2.4x on 2^20 units with the L2 warm.
+// copied with plain loads and stores.  Measured against the load/store kernels
+// on GB300: the same bytes and about the same time under ncu; back to back,
+// the flat gather 1-3 % faster on units of 202M and 2^29 elements (0.93-0.98 of
+// the copy peak) and 1.5x on 2^24, 2.4x on 2^20 units with the L2 warm, the row
+// gather 3.5 % faster on a Llama-7B layer (0.94).
 //
 // Every wait is bounded by the global timer; a wait that gives up records a
 // nonzero status in g_gather_status (read with the step kernels' word by
