@@ -35,6 +35,21 @@ def test_header_declarations_are_exported(za):
         assert hasattr(lib, n), f"{n} not exported"
 
 
+def test_binding_constants_match_the_header(za):
+    """Every numeric #define of the header has the same value in the Python binding
+    (status codes through za.ERRORS)."""
+    text = open(os.path.join(ROOT, "include", "zeroadam.h")).read()
+    defines = re.findall(r"^#define (ZERO_\w+)\s+\(?(-?(?:0x[0-9a-fA-F]+|\d+))\)?", text, flags=re.M)
+    assert len(defines) >= 25
+    errors = {v: k for k, v in za.ERRORS.items()}
+    for name, value in defines:
+        v = int(value, 0)
+        if name.startswith("ZERO_E_"):
+            assert errors[name] == v, name
+        else:
+            assert getattr(za, name) == v, name
+
+
 def test_library_links_the_shared_cuda_runtime(za):
     with open("/proc/self/maps") as f:
         maps = f.read()

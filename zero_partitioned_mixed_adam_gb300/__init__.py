@@ -20,9 +20,11 @@ LIB_PATH = os.path.join(_HERE, "libzeroadam.so")
 ZERO_OK = 0
 ZERO_ALL_RANKS = -1
 ZERO_GRAD_FULL, ZERO_GRAD_SHARD, ZERO_GRAD_WINDOW = 0, 1, 2
+ZERO_GRAD_LAYOUT_MASK = 0x0F
 ZERO_GRAD_F32, ZERO_ACC_BF16 = 0x10, 0x20
 ZERO_PARAM_FULL, ZERO_PARAM_SHARD = 0, 1
 ZERO_MAX_WORLD = 1024
+ZERO_MAX_UNIT_TENSORS = 256
 
 ERRORS = {
     -1: "ZERO_E_NULLPTR", -2: "ZERO_E_WORLD", -3: "ZERO_E_NUMEL", -4: "ZERO_E_RANK",
@@ -226,4 +228,5 @@ __all__ = ["zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_ga
            "zero3_unit_gather_rows", "rows_layout", "device_status", "test_withhold_copies",
            "ZeroPlan", "ZeroError", "strerror", "version", "raw_lib", "ZERO_ALL_RANKS",
            "ZERO_GRAD_FULL", "ZERO_GRAD_SHARD", "ZERO_GRAD_WINDOW", "ZERO_GRAD_F32",
-           "ZERO_ACC_BF16", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "EXPORTS", "LIB_PATH"]
+           "ZERO_ACC_BF16", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "ZERO_MAX_WORLD",
+           "ZERO_MAX_UNIT_TENSORS", "EXPORTS", "LIB_PATH"]
