@@ -1,0 +1,76 @@
+"""bench.py's one JSON line: every key the benchmark contract names, for the reference arm
+(the oracle on the host cores: runs on CPU) and for the library's arm (on a GPU)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+from conftest import cuda_available
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BASE = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+        "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "e2e",
+        "gpu_launches", "cpu_baseline")
+
+
+def _line(*args, timeout=600):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                       capture_output=True, text=True, timeout=timeout, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    return json.loads(lines[0])
+
+
+def _common(d, steps, warmup):
+    for k in BASE:
+        assert k in d, k
+    assert d["n_gpus"] == 1 and d["steps"] == steps and d["warmup"] == warmup
+    assert d["unit"] == "Gelem/s" and d["higher_is_better"] is True
+    assert d["scaling"] == "weak" and d["data"] == "synthetic" and d["vs_baseline"] is None
+    assert d["config"]["workload"] == "tiny" and d["value"] > 0 and d["ms_per_step"] > 0
+    e = d["e2e"]
+    for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+        assert k in e, k
+
+
+def test_reference_arm_line():
+    d = _line("--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3")
+    _common(d, 1, 3)
+    assert d["impl"] == "reference" and d["gpu_launches"] == 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_warmup_below_three_is_refused():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"],
+                       capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert r.returncode != 0
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")
+def test_our_arm_line():
+    d = _line("--workload", "tiny", "--steps", "5", "--warmup", "3", "--cpu-seconds", "1",
+              "--e2e-steps", "2")
+    _common(d, 5, 3)
+    assert "impl" not in d and d["gpu_launches"] == 5
+    r = d["roofline"]
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in r, k
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 2 * 1_000_003
+    assert e["d2h_bytes_per_step"] == 2 * 1_000_003
+    c = d["clocks"]
+    for k in ("sm_mhz", "sm_max_mhz", "reasons"):
+        assert k in c, k
+    assert d["config"]["l2"].startswith("L2 flushed")   # tiny moves less than 4 L2 sizes
