@@ -189,6 +189,23 @@ def test_ragged_sizes_all_ranks(numel, world):
         pr.check(f"{numel}/{world} t={t}")
 
 
+def test_ranks_of_padding_only_step_nothing():
+    """Psi = 17 over 16 ranks: S = 2, so ranks 9..15 own only padding.  Their single-rank
+    steps return ZERO_OK, launch nothing and leave every output as it was; ranks 0..8 step
+    their real elements as the oracle does."""
+    numel, world = 17, 16
+    for rank in range(world):
+        pr = Problem(numel, world, rank=rank, grad_layout=SHARD, seed=rank)
+        before = [x.clone() for x in (pr.w, pr.m, pr.v, pr.p)]
+        pr.step(1)
+        pr.check(f"rank {rank}")
+        if rank * pr.S >= numel:
+            assert pr.cnt == 0
+            for a, b in zip((pr.w, pr.m, pr.v, pr.p), before):
+                assert torch.equal(a, b)
+    assert za.device_status() == za.ZERO_OK
+
+
 @pytest.mark.parametrize("offs", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 5), (7, 3, 7), (4, 2, 4),
                                   (1, 1, 1)])
 def test_misaligned_buffers(offs):
