@@ -892,15 +892,18 @@ def run_zero3_prefetch(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="1p3b")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--gpus", type=int, default=1, help="GPUs (one process each under torchrun)")
+    ap.add_argument("--steps", type=int, default=50, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed steps first (>= 3)")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours",
+                    help="reference: the CPU oracle on the host cores")
+    ap.add_argument("--workload", default="1p3b",
+                    help="1p3b | gpt2 | 7b_rank3 | tiny | unit:U:N | zero2_buckets | zero3_prefetch")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run")
+    ap.add_argument("--e2e-steps", type=int, default=5, help="steps of the host-buffer run")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="seconds of oracle timing on all host cores")
     ap.add_argument("--bucket", type=int, default=1 << 24, help="zero2_buckets: elements")
     ap.add_argument("--layers", type=int, default=8, help="zero3_prefetch: units per pass")
     ap.add_argument("--prefetch-world", type=int, default=8, help="zero3_prefetch: ranks")
