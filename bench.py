@@ -685,6 +685,24 @@ def run_zero2_buckets(args):
         for i, b0 in enumerate(starts):
             step_bucket(i, b0, main_s)
 
+    # the buckets' steps touch disjoint windows, so they need no order among themselves:
+    # round-robin over two streams lets one bucket's launch start on the SMs the previous
+    # one has finished with
+    side = torch.cuda.Stream(dev)
+
+    def buckets_two_streams(stream=None, other=None):
+        stream = stream or main_s
+        other = other or side
+        tt[0] += 1
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        other.wait_event(fork)
+        for i, b0 in enumerate(starts):
+            step_bucket(i, b0, stream if i % 2 == 0 else other)
+        join = torch.cuda.Event()
+        join.record(other)
+        stream.wait_event(join)
+
     def backward_only():
         for i, b0 in enumerate(starts):
             backward_bucket(i, b0, main_s)
@@ -715,6 +733,32 @@ def run_zero2_buckets(args):
         done.record(sb)
         main_s.wait_event(done)
 
+    sb2 = torch.cuda.Stream(dev)
+
+    def overlapped_two_streams():
+        """As overlapped(), with bucket i stepped on side stream i % 2 (pool slot i % 2 is
+        always read and released by the same stream)."""
+        tt[0] += 1
+        steps = [sb, sb2]
+        free = [torch.cuda.Event(), torch.cuda.Event()]
+        start = torch.cuda.Event()
+        start.record(main_s)
+        for j in (0, 1):
+            steps[j].wait_event(start)
+            free[j].record(steps[j])
+        for i, b0 in enumerate(starts):
+            ready = torch.cuda.Event()
+            main_s.wait_event(free[i % 2])
+            backward_bucket(i, b0, main_s)
+            ready.record(main_s)
+            steps[i % 2].wait_event(ready)
+            step_bucket(i, b0, steps[i % 2])
+            free[i % 2].record(steps[i % 2])
+        for j in (0, 1):
+            done = torch.cuda.Event()
+            done.record(steps[j])
+            main_s.wait_event(done)
+
     def timed(fn):
         for _ in range(args.warmup):
             fn()
@@ -737,7 +781,16 @@ def run_zero2_buckets(args):
             for i, b0 in enumerate(starts):
                 step_bucket(i, b0, cap)
     t_graph = timed(graph.replay)
+    t_two = timed(buckets_two_streams)
+    graph2 = torch.cuda.CUDAGraph()
+    side2 = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph2, stream=cap):
+            buckets_two_streams(cap, side2)
+    t_two_graph = timed(graph2.replay)
     t_bwd, t_serial, t_over = timed(backward_only), timed(backward_then_steps), timed(overlapped)
+    t_over2 = timed(overlapped_two_streams)
     peak, peak_src = _peaks()
     nbytes = (2 * N + 26) * numel
     line = {
@@ -752,8 +805,12 @@ def run_zero2_buckets(args):
         "whole_step_ms": t_whole, "bucket_steps_ms": t_buckets,
         "small_launch_efficiency": t_whole / t_buckets,
         "bucket_steps_graph_ms": t_graph, "small_launch_efficiency_graph": t_whole / t_graph,
+        "bucket_steps_two_streams_ms": t_two,
+        "small_launch_efficiency_two_streams": t_whole / t_two,
+        "bucket_steps_two_streams_graph_ms": t_two_graph,
+        "small_launch_efficiency_two_streams_graph": t_whole / t_two_graph,
         "backward_only_ms": t_bwd, "backward_then_steps_ms": t_serial,
-        "overlapped_ms": t_over,
+        "overlapped_ms": t_over, "overlapped_two_streams_ms": t_over2,
         "hidden_fraction_of_steps": (t_serial - t_over) / t_buckets,
         "roofline": {"bound": "hbm", "achieved": nbytes / (t_buckets * 1e-3) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": nbytes / (t_buckets * 1e-3) / 1e9 / peak,

@@ -121,10 +121,13 @@ def test_single_rank_windows(layout):
     assert (dp[:lo] == 0x1234).all() and (dp[hi:] == 0x1234).all()
 
 
-def test_bucketed_schedule_on_a_side_stream():
+@pytest.mark.parametrize("step_streams", [1, 2])
+def test_bucketed_schedule_on_a_side_stream(step_streams):
     """An emulated backward pass on stream A writes bucket gradients into a pool of two
-    bucket buffers (last bucket first); stream B steps each bucket once its event fires
-    and hands the buffer back.  The result equals one whole step bit for bit."""
+    bucket buffers (last bucket first); a side stream steps each bucket once its event fires
+    and hands the buffer back -- one side stream, or two taking the buckets in turn (bucket
+    i and pool slot i % 2 on side stream i % 2).  The result equals one whole step bit for
+    bit."""
     numel, world, bucket = 2_000_003, 8, 1 << 18
     plan = za.zero_plan(numel, world)
     whole = _state(plan, numel)
@@ -135,15 +138,17 @@ def test_bucketed_schedule_on_a_side_stream():
     za.zero_adam_step(plan, -1, g, *whole, lr=LR, t=1)
     torch.cuda.synchronize()
 
-    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa = torch.cuda.Stream()
+    side = [torch.cuda.Stream() for _ in range(step_streams)]
     pool = [[torch.empty(bucket, dtype=torch.int16, device="cuda") for _ in range(world)]
             for _ in range(2)]
     free = [torch.cuda.Event() for _ in range(2)]
-    for e in free:
-        e.record(sb)
+    for slot, e in enumerate(free):
+        e.record(side[slot % step_streams])
     starts = list(range(0, numel, bucket))[::-1]
     for i, b0 in enumerate(starts):
         slot = i % 2
+        sb = side[slot % step_streams]
         n = min(bucket, numel - b0)
         ready = torch.cuda.Event()
         with torch.cuda.stream(sa):
