@@ -395,6 +395,54 @@ def run_reference(args, wl):
     return 0
 
 
+class Refused(Exception):
+    """A timed region in which a kernel gave up a bounded wait: some element of a step
+    was not updated, so its time is not the time of the step and no line is printed."""
+
+
+def device_verdict(za, dist=None, device=None) -> str:
+    """'ok' if every bounded wait of the library's kernels completed since the last
+    check (on every rank), else 'timeout'.  Synchronises the device."""
+    bad = 0.0 if za.device_status() == za.ZERO_OK else 1.0
+    if dist is not None:
+        import torch
+        x = torch.tensor([bad], dtype=torch.float64, device=device)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        bad = float(x.item())
+    return "ok" if bad == 0.0 else "timeout"
+
+
+def require_ok(verdict: str, what: str) -> str:
+    if verdict != "ok":
+        raise Refused(f"{what}: a kernel gave up a bounded wait (device status {verdict}); "
+                      "the steps did not complete and their time is not reported")
+    return verdict
+
+
+def timed_region(rep, stream, steps, t, flush=None, dist=None):
+    """The timed steps t+1 .. t+steps, each bracketed by CUDA events per launch on the
+    launching stream, with a barrier and a device synchronize on both sides.
+    Returns (last t, events, wall seconds)."""
+    import torch
+    nk = len(rep.kernels)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nk)] for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(rep.dev)
+    t_wall = time.perf_counter()
+    for i in range(steps):
+        t += 1
+        if flush is not None:
+            flush(i)
+        rep.step(t, stream, ev[i])
+    torch.cuda.synchronize(rep.dev)
+    wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    return t, ev, wall
+
+
 def aggregate(ms_local: float, elems_per_rank: int, world_size: int, dist=None, device=None):
     """Whole-job throughput of N replicas: every rank's elements over the slowest rank's
     time (max over ranks).  Returns (ms_max, Gelem/s)."""
@@ -456,27 +504,15 @@ def run_ours(args, wl):
         t += 1
         rep.step(t, stream)
     torch.cuda.synchronize(dev)
+    require_ok(device_verdict(rep.za, dist, dev), "prewarm and warm-up steps")
 
     nk = len(rep.kernels)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(nk)] for _ in range(args.steps)]
     flush = L2Flush(dev) if L2Flush.needed(rep.step_bytes(), dev) else None
     sampler = ClockSampler(local)
     sampler.start()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter()
-    for i in range(args.steps):
-        t += 1
-        if flush is not None:
-            flush(i)
-        rep.step(t, stream, ev[i])
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - t_wall
-    if dist is not None:
-        dist.barrier()
+    t, ev, wall = timed_region(rep, stream, args.steps, t, flush, dist)
     clocks = sampler.stop()
+    status = require_ok(device_verdict(rep.za, dist, dev), "timed region")
     if flush is None:
         total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1])
     else:   # the flushes sit between the steps: add up the steps' own launches
@@ -529,7 +565,7 @@ def run_ours(args, wl):
                          "median_launch_ms": dom["median_launch_ms"]},
             "kernels": per_kernel,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * nk,
-            "clocks": clocks, "wall_s_timed": wall,
+            "clocks": clocks, "wall_s_timed": wall, "device_status": status,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -620,6 +656,7 @@ def _e2e(args, rep, stream, t, dist, world_size):
             fn(t)
         e1.record(stream)
         torch.cuda.synchronize(rep.dev)
+        require_ok(device_verdict(rep.za, dist, rep.dev), f"e2e {name} leg")
         out[name] = aggregate(e0.elapsed_time(e1) / k_steps, rep.unit_elements(), world_size,
                               dist, rep.dev)
     ms, val = out["zero_copy"]
@@ -630,6 +667,7 @@ def _e2e(args, rep, stream, t, dist, world_size):
                     "parameters over NVLink-C2C",
             "copy_engine": {"value": out["copy_engine"][1], "ms_per_step": out["copy_engine"][0],
                             "mode": "cudaMemcpyAsync H2D, step, D2H on one stream"},
+            "device_status": "ok",
             "_steps": 2 * (k_steps + 1)}
 
 
@@ -791,6 +829,7 @@ def run_zero2_buckets(args):
     t_two_graph = timed(graph2.replay)
     t_bwd, t_serial, t_over = timed(backward_only), timed(backward_then_steps), timed(overlapped)
     t_over2 = timed(overlapped_two_streams)
+    status = require_ok(device_verdict(za), "zero2_buckets timed regions")
     peak, peak_src = _peaks()
     nbytes = (2 * N + 26) * numel
     line = {
@@ -820,6 +859,7 @@ def run_zero2_buckets(args):
                      "algorithmic_bytes_per_launch": (2 * N + 26) * B,
                      "avg_launch_ms": t_buckets / len(starts)},
         "gpu_launches": len(starts) * (N + 1), "e2e": None, "cpu_baseline": None,
+        "device_status": status,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -910,6 +950,7 @@ def run_zero3_prefetch(args):
     t_c = timed(lambda: [compute(li, li % 2) for li in range(L)])
     t_ser = timed(serial)
     t_pipe = timed(lambda: prefetch_pass(L, gather, compute, main_s, side))
+    status = require_ok(device_verdict(za), "zero3_prefetch timed regions")
     peak, peak_src = _peaks()
     g_gbs = 4 * U * L / (t_g * 1e-3) / 1e9
     # the library copies on the TMA engine when every tensor offset and row block is a
@@ -941,7 +982,7 @@ def run_zero3_prefetch(args):
                      "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                      "kernel": kname,
                      "algorithmic_bytes_per_launch": 4 * U, "avg_launch_ms": t_g / L},
-        "gpu_launches": L, "e2e": None, "cpu_baseline": None,
+        "gpu_launches": L, "e2e": None, "cpu_baseline": None, "device_status": status,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -970,17 +1011,21 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.workload == "zero3_prefetch":
-        return run_zero3_prefetch(args)
-    if args.workload == "zero2_buckets":
-        return run_zero2_buckets(args)
-    wl = _workload(args.workload)
-    if args.numel:
-        import dataclasses
-        wl = dataclasses.replace(wl, numel=args.numel, name=f"{wl.name}@numel={args.numel}")
-    if args.impl == "reference":
-        return run_reference(args, wl)
-    return run_ours(args, wl)
+    try:
+        if args.workload == "zero3_prefetch":
+            return run_zero3_prefetch(args)
+        if args.workload == "zero2_buckets":
+            return run_zero2_buckets(args)
+        wl = _workload(args.workload)
+        if args.numel:
+            import dataclasses
+            wl = dataclasses.replace(wl, numel=args.numel, name=f"{wl.name}@numel={args.numel}")
+        if args.impl == "reference":
+            return run_reference(args, wl)
+        return run_ours(args, wl)
+    except Refused as e:
+        print(f"bench.py: refused: {e}", file=sys.stderr, flush=True)
+        return 3
 
 
 if __name__ == "__main__":

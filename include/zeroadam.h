@@ -69,6 +69,7 @@ extern "C" {
 #define ZERO_E_RANGE (-13)  /* zero_adam_step_range: begin < 0 or end < begin       */
 #define ZERO_E_SHAPE (-14)  /* zero3_unit_gather_rows: bad tensor count or shape    */
 #define ZERO_E_TIMEOUT (-15) /* a kernel gave up a bounded wait (zero_device_status) */
+#define ZERO_E_HOOK (-16)    /* a test hook was called without ZEROADAM_TEST_HOOKS=1 */
 
 /* Largest tensor count of one zero3_unit_gather_rows unit. */
 #define ZERO_MAX_UNIT_TENSORS 256
@@ -253,10 +254,15 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
  * up (one second without progress, by the GPU's global timer) ends the launch
  * early, leaving that step's outputs incomplete, and records the fact in a
  * per-device status word.
- * Returns ZERO_OK if no wait has given up since the previous call, else
- * ZERO_E_TIMEOUT; either way the word is cleared.  ZERO_E_DEVICE if there is no
- * usable device.  Unlike the other calls this one synchronises the current
- * device (it reads device memory).
+ * The call first synchronises the current device (cudaDeviceSynchronize),
+ * so every kernel launched before it, on any stream of the device, has
+ * finished; then it reads and clears the words with one atomic exchange on the
+ * GPU each, so a word set while the call runs is reported now or by the next
+ * call, never lost.  Returns ZERO_OK if no wait has given up since the previous
+ * call, else ZERO_E_TIMEOUT.  ZERO_E_DEVICE if there is no usable device or the
+ * synchronisation reports an error (an earlier asynchronous fault; its CUDA
+ * text is in zero_strerror).  It launches a one-thread kernel on the legacy
+ * default stream, so it must not be called while a stream capture is open.
  */
 int zero_device_status(void);
 
@@ -272,7 +278,9 @@ int zero_device_status(void);
  * usable.  Launches of the other kernels are unaffected (they do not wait).  The setting is
  * process-wide and read when a step is launched.  Returns the previous
  * setting (0 or 1).  It exists so that tests can exercise the timeout path
- * without faulting or hanging a GPU; production code never calls it.
+ * without faulting or hanging a GPU; production code never calls it.  It is
+ * off unless the environment variable ZEROADAM_TEST_HOOKS is "1" when it is
+ * called; otherwise it changes nothing and returns ZERO_E_HOOK.
  */
 int zero_test_withhold_copies(int on);
 

@@ -244,3 +244,22 @@ def test_strerror(za):
         assert s and s != "unknown status"
     assert za.strerror(0) == "ok"
     assert za.version() == 0x000100
+
+
+def test_test_hook_is_off_without_its_environment_variable():
+    """zero_test_withhold_copies answers only when ZEROADAM_TEST_HOOKS=1: a process
+    without it gets ZERO_E_HOOK and the flag stays off; with it the call sets the flag
+    and returns the previous setting.  Host only (the flag is read at launch time)."""
+    import subprocess
+    import sys
+    child = ("import sys; sys.path.insert(0, %r)\n"
+             "import zero_partitioned_mixed_adam_gb300 as za\n"
+             "lib = za.raw_lib()\n"
+             "print(lib.zero_test_withhold_copies(1), lib.zero_test_withhold_copies(0))\n" % ROOT)
+    base = {k: v for k, v in os.environ.items() if k != "ZEROADAM_TEST_HOOKS"}
+    for env, want in ((base, "-16 -16"), (dict(base, ZEROADAM_TEST_HOOKS="0"), "-16 -16"),
+                      (dict(base, ZEROADAM_TEST_HOOKS="1"), "0 1")):
+        r = subprocess.run([sys.executable, "-c", child], capture_output=True, text=True,
+                           timeout=120, env=env)
+        assert r.returncode == 0, r.stderr
+        assert r.stdout.split()[-2:] == want.split(), (env.get("ZEROADAM_TEST_HOOKS"), r.stdout)

@@ -74,6 +74,42 @@ def test_withheld_copies_time_out_and_the_context_survives(world):
     assert za.device_status() == za.ZERO_OK
 
 
+@pytest.mark.parametrize("world", [8, 16])
+def test_timeout_on_a_side_stream_is_seen_without_a_torch_synchronize(world):
+    """The step runs on a non-blocking torch stream and device_status() is called
+    straight after the launch returns: the call itself must wait for the kernel
+    (it synchronises the device) and report its timeout."""
+    numel = 1_000_003
+    plan, g, w0 = _setup(numel, world)
+    state = _fresh(w0, numel)
+    torch.cuda.synchronize()
+    assert za.device_status() == za.ZERO_OK
+    side = torch.cuda.Stream()
+    prev = za.test_withhold_copies(True)
+    try:
+        za.zero_adam_step(plan, -1, g, *state, lr=1e-3, t=1, stream=side)
+        status = za.device_status()     # no torch synchronize before it
+    finally:
+        za.test_withhold_copies(prev)
+    assert status == E_TIMEOUT
+    assert za.device_status() == za.ZERO_OK
+
+
+def test_zero_adam_check_raises_on_a_given_up_wait():
+    from zero_partitioned_mixed_adam_gb300.optim import ZeroAdam
+    params = [torch.nn.Parameter(torch.randn(1 << 16, device="cuda")) for _ in range(4)]
+    opt = ZeroAdam(params, lr=1e-3, world=16)
+    opt.step(check=True)                  # completes: no error
+    prev = za.test_withhold_copies(True)
+    try:
+        with pytest.raises(za.ZeroError) as e:
+            opt.step(check=True)
+    finally:
+        za.test_withhold_copies(prev)
+    assert e.value.code == "ZERO_E_TIMEOUT"
+    opt.step(check=True)
+
+
 def test_hook_leaves_the_register_staged_kernel_alone():
     """N = 4 runs the register-staged kernel, which has no waits: the hook changes
     nothing there."""

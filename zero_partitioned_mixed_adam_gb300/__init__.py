@@ -30,7 +30,7 @@ ERRORS = {
     -1: "ZERO_E_NULLPTR", -2: "ZERO_E_WORLD", -3: "ZERO_E_NUMEL", -4: "ZERO_E_RANK",
     -5: "ZERO_E_STEP", -6: "ZERO_E_ALIGN", -7: "ZERO_E_HPARAM", -8: "ZERO_E_LAYOUT",
     -9: "ZERO_E_PLAN", -10: "ZERO_E_ALIAS", -11: "ZERO_E_LAUNCH", -12: "ZERO_E_DEVICE",
-    -13: "ZERO_E_RANGE", -14: "ZERO_E_SHAPE", -15: "ZERO_E_TIMEOUT",
+    -13: "ZERO_E_RANGE", -14: "ZERO_E_SHAPE", -15: "ZERO_E_TIMEOUT", -16: "ZERO_E_HOOK",
 }
 
 # Every symbol include/zeroadam.h declares.
@@ -204,15 +204,25 @@ def zero3_unit_gather_rows(shapes, world: int, shards, full, stream=None) -> Non
 
 def device_status() -> int:
     """ZERO_OK, or ZERO_E_TIMEOUT if a kernel gave up a bounded wait since the last call
-    (clears the word; synchronises the current device)."""
+    (synchronises the current device, then reads and clears the words)."""
     return _lib.zero_device_status()
 
 
+def check_device(what: str = "device_status") -> None:
+    """Raise ZeroError unless every bounded wait since the last check completed."""
+    rc = _lib.zero_device_status()
+    if rc != ZERO_OK:
+        raise ZeroError(rc, what)
+
+
 def test_withhold_copies(on: bool) -> bool:
-    """Test hook: while on, the TMA-staged step kernels issue no copies, so their
-    bounded waits run out (zero_device_status then reports ZERO_E_TIMEOUT).
-    Returns the previous setting."""
-    return bool(_lib.zero_test_withhold_copies(1 if on else 0))
+    """Test hook: while on, the TMA-staged kernels issue no copies, so their bounded
+    waits run out (zero_device_status then reports ZERO_E_TIMEOUT).  Needs
+    ZEROADAM_TEST_HOOKS=1 in the environment.  Returns the previous setting."""
+    rc = _lib.zero_test_withhold_copies(1 if on else 0)
+    if rc < 0:
+        raise ZeroError(rc, "zero_test_withhold_copies")
+    return bool(rc)
 
 
 def version() -> int:
@@ -225,7 +235,8 @@ def raw_lib() -> ctypes.CDLL:
 
 
 __all__ = ["zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero3_unit_gather_rows", "rows_layout", "device_status", "test_withhold_copies",
+           "zero3_unit_gather_rows", "rows_layout", "device_status", "check_device",
+           "test_withhold_copies",
            "ZeroPlan", "ZeroError", "strerror", "version", "raw_lib", "ZERO_ALL_RANKS",
            "ZERO_GRAD_FULL", "ZERO_GRAD_SHARD", "ZERO_GRAD_WINDOW", "ZERO_GRAD_F32",
            "ZERO_ACC_BF16", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "ZERO_MAX_WORLD",

@@ -728,13 +728,22 @@ cudaError_t launch_variant(const StepLaunch& L) {
 
 }  // namespace
 
+namespace {
+__device__ int g_step_status_taken;
+
+// Reads and clears the status word in one atomic exchange, so that a flag a
+// kernel still running on another stream sets is either taken now or kept
+// for the next read, never lost between a read and a separate clear.
+__global__ void take_step_status_kernel() {
+  g_step_status_taken = atomicExch(&g_step_status, 0);
+}
+}  // namespace
+
 int read_and_clear_step_status(int* status) {
-  int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_step_status, sizeof(int)) != cudaSuccess) return -1;
-  if (v != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_step_status, &zero, sizeof(int)) != cudaSuccess) return -1;
-  }
+  take_step_status_kernel<<<1, 1, 0, 0>>>();
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  int v = 0;  // the copy is ordered after the kernel on the legacy default stream
+  if (cudaMemcpyFromSymbol(&v, g_step_status_taken, sizeof(int)) != cudaSuccess) return -1;
   *status = v;
   return 0;
 }

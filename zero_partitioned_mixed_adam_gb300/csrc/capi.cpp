@@ -10,6 +10,8 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <string>
 
@@ -57,6 +59,12 @@ std::atomic<int> g_withhold{0};
 
 thread_local cudaError_t t_last_cuda = cudaSuccess;
 thread_local std::string t_msg;
+
+// ZERO_E_DEVICE, keeping the CUDA error for zero_strerror.
+int device_error(cudaError_t e) {
+  t_last_cuda = e == cudaSuccess ? cudaErrorNoDevice : e;
+  return ZERO_E_DEVICE;
+}
 
 int launch_status(cudaError_t e) {
   if (e == cudaSuccess) return ZERO_OK;
@@ -258,7 +266,11 @@ int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* gra
                     param_layout, lr, beta1, beta2, eps, t, stream);
 }
 
-int zero_test_withhold_copies(int on) { return g_withhold.exchange(on != 0 ? 1 : 0); }
+int zero_test_withhold_copies(int on) {
+  const char* gate = std::getenv("ZEROADAM_TEST_HOOKS");
+  if (gate == nullptr || std::strcmp(gate, "1") != 0) return ZERO_E_HOOK;
+  return g_withhold.exchange(on != 0 ? 1 : 0);
+}
 
 int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs,
                       void* full_bf16, void* stream) {
@@ -337,10 +349,17 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
 int zero_device_status(void) {
   Trace trace("zero_device_status");
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_E_DEVICE;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return device_error(e);
+  // Every kernel launched so far on this device, on any stream, has finished
+  // (and set its word, if a wait gave up) before the words are taken.
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return device_error(e);
+  static std::mutex mu;  // one caller at a time takes the words
+  std::lock_guard<std::mutex> lock(mu);
   int step = 0, gather = 0;
-  if (read_and_clear_step_status(&step) != 0) return ZERO_E_DEVICE;
-  if (read_and_clear_gather_status(&gather) != 0) return ZERO_E_DEVICE;
+  if (read_and_clear_step_status(&step) != 0) return device_error(cudaGetLastError());
+  if (read_and_clear_gather_status(&gather) != 0) return device_error(cudaGetLastError());
   return step == 0 && gather == 0 ? ZERO_OK : ZERO_E_TIMEOUT;
 }
 
@@ -357,10 +376,14 @@ const char* zero_strerror(int status) {
     case ZERO_E_LAYOUT: return "unknown layout, or a shard layout with ZERO_ALL_RANKS";
     case ZERO_E_PLAN: return "plan fields differ from zero_plan(numel, world)";
     case ZERO_E_ALIAS: return "an output buffer overlaps another buffer";
-    case ZERO_E_DEVICE: return "no usable CUDA device";
+    case ZERO_E_DEVICE:
+      t_msg = std::string("no usable CUDA device, or the device reported an error: ") +
+              cudaGetErrorString(t_last_cuda == cudaSuccess ? cudaErrorNoDevice : t_last_cuda);
+      return t_msg.c_str();
     case ZERO_E_RANGE: return "the window must satisfy 0 <= begin <= end";
     case ZERO_E_SHAPE: return "ntensors in [1, ZERO_MAX_UNIT_TENSORS] and sizes >= 1 required";
     case ZERO_E_TIMEOUT: return "a kernel gave up a bounded wait; that step's outputs are incomplete";
+    case ZERO_E_HOOK: return "test hooks are off: they need ZEROADAM_TEST_HOOKS=1 in the environment";
     case ZERO_E_LAUNCH:
       t_msg = std::string("kernel launch failed: ") + cudaGetErrorString(t_last_cuda);
       return t_msg.c_str();

@@ -537,13 +537,20 @@ cudaError_t launch_unit_gather_rows(const GatherRowsLaunch& L) {
   return launch_rows_cap<1024>(L);
 }
 
+namespace {
+__device__ int g_gather_status_taken;
+
+// As take_step_status_kernel: one atomic exchange reads and clears the word.
+__global__ void take_gather_status_kernel() {
+  g_gather_status_taken = atomicExch(&g_gather_status, 0);
+}
+}  // namespace
+
 int read_and_clear_gather_status(int* status) {
-  int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_gather_status, sizeof(int)) != cudaSuccess) return -1;
-  if (v != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_gather_status, &zero, sizeof(int)) != cudaSuccess) return -1;
-  }
+  take_gather_status_kernel<<<1, 1, 0, 0>>>();
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  int v = 0;  // the copy is ordered after the kernel on the legacy default stream
+  if (cudaMemcpyFromSymbol(&v, g_gather_status_taken, sizeof(int)) != cudaSuccess) return -1;
   *status = v;
   return 0;
 }

@@ -20,7 +20,7 @@ from __future__ import annotations
 
 import torch
 
-from . import ZERO_ALL_RANKS, zero_adam_step, zero_plan
+from . import ZERO_ALL_RANKS, check_device, zero_adam_step, zero_plan
 
 
 class ZeroAdam:
@@ -60,13 +60,19 @@ class ZeroAdam:
             off += p.numel()
         return out
 
-    def step(self, stream=None):
-        """One ZeRO-2 step of every rank: reduce-scatter + average, Adam, all-gather."""
+    def step(self, stream=None, check=False):
+        """One ZeRO-2 step of every rank: reduce-scatter + average, Adam, all-gather.
+
+        With check=True the call waits for the device and raises ZeroError
+        (ZERO_E_TIMEOUT) if a kernel gave up a bounded wait, i.e. if some element
+        of the step was not updated."""
         self.t += 1
         b1, b2 = self.betas
         zero_adam_step(self.plan, ZERO_ALL_RANKS, self.grads, self.master, self.m, self.v,
                        self.flat_params, lr=self.lr, beta1=b1, beta2=b2, eps=self.eps, t=self.t,
                        stream=stream)
+        if check:
+            check_device("ZeroAdam.step")
 
     def zero_grad(self):
         for g in self.grads:
