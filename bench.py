@@ -996,7 +996,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours",
                     help="reference: the CPU oracle on the host cores")
     ap.add_argument("--workload", default="1p3b",
-                    help="1p3b | gpt2 | 7b_rank3 | tiny | unit:U:N | zero2_buckets | zero3_prefetch")
+                    help="1p3b | gpt2 | 7b_rank3 | 7b_rank3_prewarm | tiny | unit:U:N | "
+                         "zero2_buckets | zero3_prefetch")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run")
     ap.add_argument("--e2e-steps", type=int, default=5, help="steps of the host-buffer run")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")

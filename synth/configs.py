@@ -11,7 +11,8 @@ Sizes only and draw recipes: no optimizer arithmetic lives here.
             5 prior steps, timed from t = 6.
   7b_rank3  Psi = 7e9 (Llama-style 7B), N = 8, rank 3 only: 8 bf16 gradient slices of its
             875M-element shard, fp32 master/m/v of the shard, bf16 output into the full
-            7e9-element parameter buffer.
+            7e9-element parameter buffer.  7b_rank3_prewarm: the same with m and v from
+            5 prior steps, timed from t = 6.
   unit      ZeRO-3 units of U in {2^20, 2^24, 202,383,360 (one Llama-7B layer), 2^29} elements,
             N in {2, 8, 64}: gather the N bf16 parameter shards, then rank 0's step on its
             shard from N bf16 gradient slices.
@@ -89,6 +90,9 @@ B1P3 = StepWorkload("1p3b", numel=1_300_000_000, world=16, steps=1, prewarm=5,
                     grad_dist=STUDENT_T3, outlier_rate=1e-6, outlier_value=1e2)
 B7_RANK3 = StepWorkload("7b_rank3", numel=7_000_000_000, world=8, rank=3, grad_layout="shard",
                         steps=1)
+# the same rank with five steps of moment history before the first timed step
+B7_RANK3_PREWARM = StepWorkload("7b_rank3_prewarm", numel=7_000_000_000, world=8, rank=3,
+                                grad_layout="shard", steps=1, prewarm=5)
 
 assert TINY.numel == 1_000_003 and TINY.shard == 250_001
 assert GPT2.numel == 124_439_808 and GPT2.shard == 15_554_976
@@ -110,4 +114,4 @@ def unit_shard_spec(unit_numel: int, world: int, r: int) -> Spec:
     return Spec(seed=unit_numel % 1000003 + world, stream=STREAM_PARAM_SHARD, rank=r, sigma=0.02)
 
 
-WORKLOADS = {w.name: w for w in (TINY, GPT2, B1P3, B7_RANK3)}
+WORKLOADS = {w.name: w for w in (TINY, GPT2, B1P3, B7_RANK3, B7_RANK3_PREWARM)}

@@ -132,3 +132,103 @@ def oracle_step_parallel(numel, world, rank, grads, master, m, v, param, lr, b1,
 
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(run, range(len(bounds) - 1)))
+
+
+# ------------------------------------------------- full-size parity on sampled windows
+
+CHUNK = 1 << 24   # random chunks compared element by element
+EDGE = 1 << 20    # elements compared at the start and the end of every rank's range
+HALO = 16         # elements compared on each side of every shard or unit boundary
+
+
+def sample_windows(lo, hi, rank_ranges, rng, n_chunks=3, chunk=CHUNK, edge=EDGE, halo=HALO,
+                   boundaries=()):
+    """Global index windows [a, b) inside [lo, hi) that a full-size parity test compares:
+    every element of `n_chunks` random `chunk`-element chunks, the first and last `edge`
+    elements of each rank range, and every index within `halo` of a boundary (each rank
+    range's ends and `boundaries`).  Overlapping or touching windows are merged."""
+    ws = []
+    for a, b in rank_ranges:
+        a, b = max(lo, a), min(hi, b)
+        if b > a:
+            ws += [(a, min(b, a + edge)), (max(a, b - edge), b)]
+    for x in [a for a, _ in rank_ranges] + [b for _, b in rank_ranges] + list(boundaries):
+        ws.append((max(lo, x - halo), min(hi, x + halo)))
+    for _ in range(n_chunks):
+        a = int(rng.integers(lo, max(lo + 1, hi - chunk + 1)))
+        ws.append((a, min(hi, a + chunk)))
+    ws = sorted((a, b) for a, b in ws if b > a)
+    merged = []
+    for a, b in ws:
+        if merged and a <= merged[-1][1]:
+            merged[-1] = (merged[-1][0], max(merged[-1][1], b))
+        else:
+            merged.append((a, b))
+    return merged
+
+
+def window_elements(windows):
+    return sum(b - a for a, b in windows)
+
+
+class WindowOracle:
+    """The oracle's state on a set of global index windows of one workload, stepped
+    with the same gradient bytes the device saw.  Initial master weights come from the
+    host generator; moments start at zero."""
+
+    def __init__(self, numel, world, rank, windows, master_spec, hparams):
+        self.numel, self.world, self.rank = numel, world, rank
+        self.windows = windows
+        self.hp = hparams
+        self.w = [synth.fill_host(master_spec, a, b - a, synth.OUT_F32) for a, b in windows]
+        self.m = [np.zeros(b - a, np.float32) for a, b in windows]
+        self.v = [np.zeros(b - a, np.float32) for a, b in windows]
+        self.p = [np.zeros(b - a, np.uint16) for a, b in windows]
+
+    def step(self, t, grads, threads=16, sub=1 << 20):
+        """grads[j][k]: rank k's bf16 gradient on window j (uint16, the window's length)."""
+        from concurrent.futures import ThreadPoolExecutor
+        lr, b1, b2, eps = self.hp
+        jobs = []
+        for j, (a, b) in enumerate(self.windows):
+            for i0 in range(a, b, sub):
+                jobs.append((j, i0, min(b, i0 + sub)))
+
+        def run(job):
+            j, i0, i1 = job
+            a = self.windows[j][0]
+            oracle.zero_step(self.numel, self.world, self.rank, grads[j], self.w[j], self.m[j],
+                             self.v[j], self.p[j], lr, b1, b2, eps, t, i0=i0, i1=i1,
+                             grad_base=a, state_base=a, param_base=a)
+
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(run, jobs))
+
+    def compare(self, master, m, v, param, state_first, param_first, what):
+        """Device state (index = global - state_first) and bf16 parameters (index =
+        global - param_first) against the oracle on every window."""
+        for j, (a, b) in enumerate(self.windows):
+            s = slice(a - state_first, b - state_first)
+            ps = slice(a - param_first, b - param_first)
+            tag = f"{what} [{a},{b})"
+            assert_f32_close(to_host_f32(master[s]), self.w[j], f"{tag} master")
+            assert_f32_close(to_host_f32(m[s]), self.m[j], f"{tag} m")
+            assert_f32_close(to_host_f32(v[s]), self.v[j], f"{tag} v")
+            assert_bf16_close(to_host_u16(param[ps]), self.p[j], f"{tag} param")
+
+
+def device_grad_windows(grads, windows, first, specs=None, check_every=4, seed=0):
+    """Host copies of the device gradient buffers on each window (buffer index = global -
+    first): out[j][k].  With specs (rank k's generator recipe, indexed by global
+    position), some windows' bytes are spot-checked against the host generator."""
+    out = []
+    for j, (a, b) in enumerate(windows):
+        row = []
+        for k, g in enumerate(grads):
+            h = to_host_u16(g[a - first:b - first]).copy()
+            if specs is not None and (j + k) % check_every == 0:
+                spot_check_generated(h, specs[k], a, synth.OUT_BF16, samples=256,
+                                     seed=seed + 31 * j + k)
+            row.append(h)
+        out.append(row)
+    return out

@@ -1,10 +1,10 @@
 """ZeRO-3 unit gather and the per-unit step (through the C ABI) against the oracle.
 
-The gather is a copy, so the bar is bit-exactness.  Small cases compare the
-whole unit; the unit sweep (U up to 2^29, N in {2, 8, 64}) compares the whole
-unit with an independent device concatenation and the oracle on windows that
-cover every shard boundary.  The unit step is rank 0's step on its shard from
-N gradient slices, writing its bf16 shard.
+The gather is a copy, so the bar is bit-exactness.  Every case, the unit sweep
+(U up to 2^29, N in {2, 8, 64}) included, compares the whole gathered unit with
+the oracle's gather of the same shard bytes.  The unit step is rank 0's step
+on its shard from N gradient slices, writing its bf16 shard, compared with the
+oracle on sampled windows over two steps.
 """
 import numpy as np
 import pytest
@@ -78,62 +78,49 @@ def test_gather_misaligned(off_src, off_dst):
 @pytest.mark.parametrize("N", C.UNIT_WORLDS)
 def test_unit_sweep_gather_and_step(U, N):
     """The sweep's configuration: gather the N parameter shards, then rank 0's step on
-    its shard from N gradient slices (ZERO_GRAD_SHARD, ZERO_PARAM_SHARD)."""
+    its shard from N gradient slices (ZERO_GRAD_SHARD, ZERO_PARAM_SHARD), two steps.
+
+    The whole gathered unit is compared with the oracle's gather of the same shard
+    bytes (host copies of the device generator's output, spot-checked against the host
+    generator).  The step is compared with the oracle after t = 1 and t = 2 on the
+    sampled windows of rank 0's shard: every element of 3 random 2^24 chunks, the first
+    and last 2^20 elements, +-16 around its ends."""
     plan, bases, shards = _shards_dev(U, N)
     S = plan.shard
     full = torch.empty(U, dtype=torch.int16, device="cuda")
     za.zero3_unit_gather(plan, shards, full)
-    # an independent device concatenation (torch) of the same shards
-    cat = torch.cat(shards)[:U]
-    assert torch.equal(full, cat)
-    # the oracle on windows around every shard boundary and at both ends
     torch.cuda.synchronize()
-    wins = [(0, min(U, 64)), (max(0, U - 64), U)]
-    for r in range(1, N):
-        b = r * S
-        if b < U:
-            wins.append((b - 8, min(U, b + 8)))
-    host_sh = [synth.fill_host(C.unit_shard_spec(U, N, r), 0, S, synth.OUT_BF16) for r in range(N)] \
-        if U * 1 <= (1 << 24) else None
-    if host_sh is not None:
-        ref = oracle.unit_gather(U, N, host_sh)
-        assert (gu.to_host_u16(full) == ref).all()
-    else:
-        for a, b in wins:
-            # element i of the unit comes from shard i // S at i % S
-            exp = np.array([synth.fill_host(C.unit_shard_spec(U, N, i // S), i % S, 1,
-                                            synth.OUT_BF16)[0] for i in range(a, b)], np.uint16)
-            assert (gu.to_host_u16(full[a:b]) == exp).all(), (a, b)
-    del full, cat, bases, shards
+    host_sh = []
+    for r, sh in enumerate(shards):
+        h = gu.to_host_u16(sh)
+        gu.spot_check_generated(h, C.unit_shard_spec(U, N, r), 0, synth.OUT_BF16, samples=256,
+                                seed=r)
+        host_sh.append(h)
+    ref = oracle.unit_gather(U, N, host_sh)
+    assert (gu.to_host_u16(full) == ref).all()
+    del full, bases, shards, host_sh, ref
 
     # rank 0's step on its shard
     wl = C.unit_workload(U, N)
     g = [torch.empty(S, dtype=torch.int16, device="cuda") for _ in range(N)]
-    for k in range(N):
-        gu.dev_fill_into(g[k], wl.grad_spec(k, 1), 0, synth.OUT_BF16)
     w = torch.empty(S, dtype=torch.float32, device="cuda")
     gu.dev_fill_into(w, wl.master_spec(), 0, synth.OUT_F32)
     m = torch.zeros_like(w)
     v = torch.zeros_like(w)
     p = torch.full((S,), 0x1234, dtype=torch.int16, device="cuda")
-    za.zero_adam_step(plan, 0, g, w, m, v, p, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
-                      eps=wl.eps, t=1, grad_layout=za.ZERO_GRAD_SHARD,
-                      param_layout=za.ZERO_PARAM_SHARD)
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(U + N)
-    for a in sorted({0, max(0, S - 1024), int(rng.integers(0, max(1, S - 1024)))}):
-        b = min(S, a + 1024)
-        hg = [synth.fill_host(wl.grad_spec(k, 1), a, b - a, synth.OUT_BF16) for k in range(N)]
-        hw = synth.fill_host(wl.master_spec(), a, b - a, synth.OUT_F32)
-        hm = np.zeros(b - a, np.float32)
-        hv = np.zeros(b - a, np.float32)
-        hp = np.zeros(b - a, np.uint16)
-        oracle.zero_step(U, N, 0, hg, hw, hm, hv, hp, wl.lr, wl.beta1, wl.beta2, wl.eps, 1,
-                         i0=a, i1=b, grad_base=a, state_base=a, param_base=a)
-        gu.assert_f32_close(gu.to_host_f32(w[a:b]), hw, f"unit {U}/{N} master [{a},{b})")
-        gu.assert_f32_close(gu.to_host_f32(m[a:b]), hm, f"unit {U}/{N} m [{a},{b})")
-        gu.assert_f32_close(gu.to_host_f32(v[a:b]), hv, f"unit {U}/{N} v [{a},{b})")
-        gu.assert_bf16_close(gu.to_host_u16(p[a:b]), hp, f"unit {U}/{N} param [{a},{b})")
+    wins = gu.sample_windows(0, S, [(0, min(S, U))], np.random.default_rng(U + N))
+    wo = gu.WindowOracle(U, N, 0, wins, wl.master_spec(), (wl.lr, wl.beta1, wl.beta2, wl.eps))
+    for t in (1, 2):
+        for k in range(N):
+            gu.dev_fill_into(g[k], wl.grad_spec(k, t), 0, synth.OUT_BF16)
+        za.zero_adam_step(plan, 0, g, w, m, v, p, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                          eps=wl.eps, t=t, grad_layout=za.ZERO_GRAD_SHARD,
+                          param_layout=za.ZERO_PARAM_SHARD)
+        wo.step(t, gu.device_grad_windows(g, wins, 0, [wl.grad_spec(k, t) for k in range(N)],
+                                          check_every=16, seed=t))
+        torch.cuda.synchronize()
+        wo.compare(w, m, v, p, 0, 0, f"unit {U}/{N} t={t}")
+    assert za.device_status() == za.ZERO_OK
     del g, w, m, v, p
     torch.cuda.empty_cache()
 
