@@ -160,11 +160,12 @@ class Replica:
     Step workloads: one zero_adam_step.  Unit workloads (ZeRO-3): the unit
     gather of the N parameter shards, then rank 0's step on its shard."""
 
-    def __init__(self, wl, dev):
+    def __init__(self, wl, dev, unit_mode="fused"):
         import torch
         import synth
         import zero_partitioned_mixed_adam_gb300 as za
         self.za, self.wl, self.dev = za, wl, dev
+        self.unit_mode = unit_mode
         self.plan = plan = za.zero_plan(wl.numel, wl.world)
         S, P = plan.shard, plan.padded
         single = wl.rank >= 0
@@ -191,11 +192,15 @@ class Replica:
                 synth.fill_dev(C.unit_shard_spec(wl.numel, wl.world, r), 0, S, synth.OUT_BF16,
                                self.shards[r].data_ptr(), st)
             self.full = torch.empty(wl.numel, dtype=torch.int16, device=dev)
-        # (name, algorithmic bytes) of the step's launches, in order
+        # (name, algorithmic bytes) of the step's timed calls, in order
         self.kernels = []
-        if self.unit:
-            self.kernels.append((self.gather_kernel_name(), 4 * wl.numel))
-        self.kernels.append((self.step_kernel_name(), _bytes_per_step(wl, plan)))
+        if self.unit and self.unit_mode == "fused":
+            self.kernels.append((self.unit_step_kernel_name(),
+                                 4 * wl.numel + _bytes_per_step(wl, plan)))
+        else:
+            if self.unit:
+                self.kernels.append((self.gather_kernel_name(), 4 * wl.numel))
+            self.kernels.append((self.step_kernel_name(), _bytes_per_step(wl, plan)))
 
     def gather_kernel_name(self):
         """The library copies on the TMA engine when the shard is a multiple of 8
@@ -204,13 +209,25 @@ class Replica:
                and all(x.data_ptr() % 16 == 0 for x in self.shards + [self.full]))
         return "zero3_unit_gather_tma_kernel" if tma else "zero3_unit_gather_kernel"
 
+    def unit_step_kernel_name(self):
+        """zero3_unit_step runs the gather and the step as one launch when the shard
+        is a multiple of 8 elements and every buffer is 16-byte aligned at its first
+        element; otherwise the gather kernel, then the step kernel."""
+        aligned = all(x.data_ptr() % 16 == 0
+                      for x in self.shards + [self.full] + self.g + [self.w, self.m, self.v,
+                                                                     self.p])
+        if self.wl.numel >= 8 and self.n >= 8 and self.plan.shard % 8 == 0 and aligned:
+            return "zero3_unit_step_kernel"
+        return f"{self.gather_kernel_name()}+{self.step_kernel_name()}"
+
     def step_kernel_name(self):
         """The library runs a TMA-staged kernel for N = 16 (gradients and state
-        staged) and N = 8 (gradients staged) when every buffer is 16-byte aligned
-        at the range's first element (whole cudaMalloc buffers)."""
+        staged) and every other N >= 5 (gradients staged in rank groups) when
+        every buffer is 16-byte aligned at the range's first element (whole
+        cudaMalloc buffers); the register-staged kernel otherwise."""
         def aligned(t, first, esize):
             return (t.data_ptr() + first * esize) % 16 == 0
-        tma = (self.wl.world in (8, 16) and self.n >= 8
+        tma = (self.wl.world >= 5 and self.n >= 8
                and all(aligned(g, self.g_first, 2) for g in self.g)
                and all(aligned(x, 0, 4) for x in (self.w, self.m, self.v))
                and aligned(self.p, self.p_first, 2))
@@ -231,6 +248,18 @@ class Replica:
         grads/shards/param override the device buffers (host-resident inputs)."""
         za, wl = self.za, self.wl
         i = 0
+        if self.unit and self.unit_mode == "fused":
+            if ev is not None:
+                ev[0][0].record(stream)
+            za.zero3_unit_step(self.plan, wl.rank, shards or self.shards, self.full,
+                               grads or self.g, self.w, self.m, self.v,
+                               param if param is not None else self.p, lr=wl.lr,
+                               beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, t=t,
+                               grad_layout=za.ZERO_GRAD_SHARD, param_layout=za.ZERO_PARAM_SHARD,
+                               stream=stream)
+            if ev is not None:
+                ev[0][1].record(stream)
+            return
         if self.unit:
             if ev is not None:
                 ev[i][0].record(stream)
@@ -472,7 +501,9 @@ def _config(wl, rep, flush=None):
         c["bytes_per_step"] = rep.step_bytes()
         c["launches_per_step"] = [k for k, _ in rep.kernels]
         if rep.unit:
-            c["unit_step"] = "zero3_unit_gather of the N shards + rank 0's step on its shard"
+            c["unit_step"] = ("zero3_unit_step: the gather of the N shards and rank 0's step on "
+                              "its shard in one call" if rep.unit_mode == "fused" else
+                              "zero3_unit_gather of the N shards, then rank 0's step on its shard")
             c["elements"] = "unit elements U per step"
     return c
 
@@ -492,7 +523,7 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    rep = Replica(wl, dev)
+    rep = Replica(wl, dev, args.unit_mode)
     stream = torch.cuda.current_stream(dev)
     # prewarm steps (state as after t = 1..prewarm), then the timed gradients
     t = 0
@@ -530,7 +561,11 @@ def run_ours(args, wl):
     peak, peak_src = _peaks()
     traffic = None
     src, units = None, 0
-    if dom["kernel"].startswith("zero_adam_step"):
+    if dom["kernel"] == "zero3_unit_step_kernel":
+        src, units = "adam_step.cu", wl.numel         # per unit element
+    elif "+" in dom["kernel"]:
+        src = None                                    # two launches: no single capture
+    elif dom["kernel"].startswith("zero_adam_step"):
         src, units = "adam_step.cu", rep.n            # per stepped element
     elif dom["kernel"].startswith("zero3_unit_gather"):
         src, units = "unit_gather.cu", wl.numel       # per unit element
@@ -564,7 +599,8 @@ def run_ours(args, wl):
                          "avg_launch_ms": dom["avg_launch_ms"],
                          "median_launch_ms": dom["median_launch_ms"]},
             "kernels": per_kernel,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * nk,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * sum(2 if "+" in k else 1 for k, _ in rep.kernels),
             "clocks": clocks, "wall_s_timed": wall, "device_status": status,
         }
         print(json.dumps(line), flush=True)
@@ -1007,6 +1043,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=8, help="zero3_prefetch: units per pass")
     ap.add_argument("--prefetch-world", type=int, default=8, help="zero3_prefetch: ranks")
     ap.add_argument("--tokens", type=int, default=4096, help="zero3_prefetch: GEMM rows")
+    ap.add_argument("--unit-mode", choices=("fused", "separate"), default="fused",
+                    help="unit workloads: one zero3_unit_step call, or the gather and the "
+                         "step as two calls")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the workload's parameter count (smaller profiling cases)")
     args = ap.parse_args(argv)

@@ -22,7 +22,8 @@
  *     of its bounded waits gives up (see zero_device_status).  Faults inside a
  *     launched kernel surface, as for any CUDA work, at the caller's next sync.
  *   - Tracing: zero_adam_step, zero_adam_step_range, zero3_unit_gather,
- *     zero3_unit_gather_rows and zero_device_status each open an NVTX range
+ *     zero3_unit_gather_rows, zero3_unit_step and zero_device_status each
+ *     open an NVTX range
  *     named after the function for the duration of the call (visible to
  *     Nsight tools and any NVTX injection library; free when none is
  *     attached).
@@ -245,6 +246,35 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
                            int32_t world, const void* const* shard_ptrs, void* full_bf16,
                            void* stream);
 
+/*
+ * One ZeRO-3 unit's gather and one rank's step in a single launch ("ZeRO-3 and
+ * FSDP": a unit's parameters are all-gathered from the ranks' shards before
+ * the unit is used, and each rank updates only its own shard).  The result is
+ * exactly that of
+ *   zero3_unit_gather(unit_plan, shard_ptrs, full_bf16, stream);
+ *   zero_adam_step(unit_plan, rank, grad_ptrs, grad_layout, master, m, v,
+ *                  param_bf16, param_layout, lr, beta1, beta2, eps, t, stream);
+ * with the same arguments, layouts and errors as those two calls.  The step
+ * does not read the gathered unit, so the two parts run side by side in one
+ * grid instead of one after the other (one launch, overlapped ramps: the
+ * page's small units are latency-bound).  Because they overlap, the buffers
+ * of the two parts must be disjoint: full_bf16 must not overlap any gradient
+ * or any step output, and no shard may overlap a step output (ZERO_E_ALIAS).
+ * To update the rank's own bf16 shard in place (param_bf16 inside
+ * shard_ptrs[rank]) call the two functions in sequence instead.
+ *
+ * When the shard is a multiple of 8 elements, every buffer of both parts is
+ * 16-byte aligned at its first element, the gradients are bf16 and the sum is
+ * fp32, the single launch runs (bulk copies on the TMA engine, bounded waits
+ * reported by zero_device_status); otherwise the two kernels are launched in
+ * order on the stream.  Errors: those of zero3_unit_gather and
+ * zero_adam_step (ZERO_GRAD_WINDOW is not accepted: ZERO_E_LAYOUT).
+ */
+int zero3_unit_step(const zero_plan_t* unit_plan, int32_t rank, const void* const* shard_ptrs,
+                    void* full_bf16, const void* const* grad_ptrs, int32_t grad_layout,
+                    float* master, float* m, float* v, void* param_bf16, int32_t param_layout,
+                    double lr, double beta1, double beta2, double eps, int64_t t, void* stream);
+
 /* ------------------------------------------------------------------ misc */
 
 /*
@@ -269,14 +299,17 @@ int zero_device_status(void);
 /*
  * Test hook for the bounded waits; the pages' method has no counterpart.
  * While `on` is nonzero, every step launch that uses a TMA-staged kernel
- * (world 8 or 16, bf16 gradients, fp32 sum, all buffers 16-byte aligned at
- * the stepped range's first element) and every zero3_unit_gather or
- * zero3_unit_gather_rows that uses the TMA copy (see those calls) tells its
- * producers to issue no copies.  Every wait then runs out after its
- * limit (about one second), no output of that call is written, and
- * zero_device_status reports ZERO_E_TIMEOUT; the device and its context stay
- * usable.  Launches of the other kernels are unaffected (they do not wait).  The setting is
- * process-wide and read when a step is launched.  Returns the previous
+ * (world >= 5, bf16 gradients, fp32 sum, all buffers 16-byte aligned at the
+ * stepped range's first element), every zero3_unit_gather or
+ * zero3_unit_gather_rows that uses the TMA copy (see those calls), and every
+ * zero3_unit_step that runs as a single launch tells its producers to issue
+ * no copies.  Every wait then runs out after its limit (about one second),
+ * the outputs of the parts that wait are not written (at world <= 4 the
+ * unit step's step part reads its gradients without staging and completes),
+ * and zero_device_status reports ZERO_E_TIMEOUT; the device and its context
+ * stay usable.  Launches of the other kernels are unaffected (they do not
+ * wait).  The setting is process-wide and read when a call launches.  Returns
+ * the previous
  * setting (0 or 1).  It exists so that tests can exercise the timeout path
  * without faulting or hanging a GPU; production code never calls it.  It is
  * off unless the environment variable ZEROADAM_TEST_HOOKS is "1" when it is

@@ -206,6 +206,39 @@ def test_gather_argument_errors(za):
                                  None) == codes["ZERO_E_ALIAS"]
 
 
+def test_unit_step_argument_errors(za):
+    """zero3_unit_step checks both parts as their own calls do, and that the parts'
+    buffers are disjoint (they run side by side); every error is found on the host,
+    before any CUDA call, so these fake addresses are never touched."""
+    plan = za.zero_plan(1000, 4)          # shard 250
+    lib = za.raw_lib()
+    codes = {v: k for k, v in za.ERRORS.items()}
+    shards = [BASE + k * 2**20 for k in range(4)]
+    grads = [BASE + 5 * 2**30 + k * 2**28 for k in range(4)]
+    W, M, V, P, FULL = (BASE + 2**30, BASE + 2 * 2**30, BASE + 3 * 2**30, BASE + 4 * 2**30,
+                        BASE + 6 * 2**30)
+
+    def call(rank=1, full=FULL, sh=shards, g=grads, master=W, param=P, layout=1, player=1,
+             t=1, p=plan):
+        sp = (ctypes.c_void_p * 4)(*sh)
+        gp = (ctypes.c_void_p * 4)(*g)
+        return lib.zero3_unit_step(ctypes.byref(p) if p is not None else None, rank, sp, full,
+                                   gp, layout, master, M, V, param, player, 1e-3, .9, .999,
+                                   1e-8, t, None)
+
+    assert call(p=None) == codes["ZERO_E_NULLPTR"]
+    assert call(full=0) == codes["ZERO_E_NULLPTR"]
+    assert call(rank=4) == codes["ZERO_E_RANK"]
+    assert call(t=0) == codes["ZERO_E_STEP"]
+    assert call(layout=2) == codes["ZERO_E_LAYOUT"]          # no window layout
+    assert call(full=FULL + 1) == codes["ZERO_E_ALIGN"]
+    assert call(full=shards[2] + 16) == codes["ZERO_E_ALIAS"]   # the gather's own check
+    assert call(full=P - 100) == codes["ZERO_E_ALIAS"]          # unit over the step's params
+    assert call(full=grads[3] + 64) == codes["ZERO_E_ALIAS"]    # unit over a gradient
+    assert call(param=shards[1] + 2) == codes["ZERO_E_ALIAS"]   # a step output over a shard
+    assert call(master=shards[3]) == codes["ZERO_E_ALIAS"]
+
+
 def test_gather_rows_argument_errors(za):
     lib = za.raw_lib()
     codes = {v: k for k, v in za.ERRORS.items()}

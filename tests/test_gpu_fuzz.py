@@ -32,7 +32,7 @@ def _step_cases(n=48, seed=20261202):
         rank = -1 if rng.random() < 0.5 else int(rng.integers(0, world))
         gl = FULL if rank < 0 or rng.random() < 0.5 else SHARD
         pl = FULL if rank < 0 or rng.random() < 0.6 else SHARD
-        # half the cases fully aligned (the staged kernels at N = 8 and 16), half not
+        # half the cases fully aligned (the staged kernels at N >= 5), half not
         offs = (0, 0, 0) if rng.random() < 0.5 else tuple(int(x) for x in rng.integers(0, 8, 3))
         cases.append((numel, world, rank, gl, pl, offs, i))
     return cases

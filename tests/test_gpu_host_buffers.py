@@ -1,8 +1,8 @@
 """The end-to-end path with host buffers: gradients in pinned host memory and the
 bf16 parameters written to pinned host memory, read and written by the kernels
 directly (NVLink-C2C on GB300).  The result must equal the all-device step bit
-for bit, on the register-staged kernel (N = 4) and the TMA-staged ones (N = 8,
-gradients staged; N = 16, gradients and state staged)."""
+for bit, on the register-staged kernel (N = 4) and the TMA-staged ones (N = 8 and
+N = 64, gradients staged in rank groups; N = 16, gradients and state staged)."""
 import pytest
 import torch
 
@@ -16,7 +16,7 @@ pytestmark = [pytest.mark.gpu,
 import zero_partitioned_mixed_adam_gb300 as za  # noqa: E402
 
 
-@pytest.mark.parametrize("world", [4, 8, 16])
+@pytest.mark.parametrize("world", [4, 8, 16, 64])
 def test_host_resident_gradients_and_parameters(world):
     numel = 3_000_017
     plan = za.zero_plan(numel, world)

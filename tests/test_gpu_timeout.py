@@ -42,7 +42,7 @@ def _bits(x):
     return x.view(torch.int32) if x.dtype == torch.float32 else x
 
 
-@pytest.mark.parametrize("world", [8, 16])
+@pytest.mark.parametrize("world", [5, 8, 16, 64, 100])
 def test_withheld_copies_time_out_and_the_context_survives(world):
     numel = 1_000_003
     plan, g, w0 = _setup(numel, world)

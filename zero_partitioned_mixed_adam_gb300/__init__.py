@@ -35,8 +35,8 @@ ERRORS = {
 
 # Every symbol include/zeroadam.h declares.
 EXPORTS = ("zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero3_unit_gather_rows", "zero_device_status", "zero_test_withhold_copies",
-           "zero_strerror", "zero_version")
+           "zero3_unit_gather_rows", "zero3_unit_step", "zero_device_status",
+           "zero_test_withhold_copies", "zero_strerror", "zero_version")
 
 
 class ZeroError(RuntimeError):
@@ -82,6 +82,9 @@ def _load() -> ctypes.CDLL:
     lib.zero_adam_step_range.restype = ctypes.c_int
     lib.zero3_unit_gather.argtypes = [ctypes.POINTER(ZeroPlan), vp, vp, vp]
     lib.zero3_unit_gather.restype = ctypes.c_int
+    lib.zero3_unit_step.argtypes = [ctypes.POINTER(ZeroPlan), i32, vp, vp, vp, i32, vp, vp, vp,
+                                    vp, i32, dbl, dbl, dbl, dbl, i64, vp]
+    lib.zero3_unit_step.restype = ctypes.c_int
     lib.zero3_unit_gather_rows.argtypes = [i32, vp, vp, i32, vp, vp, vp]
     lib.zero3_unit_gather_rows.restype = ctypes.c_int
     lib.zero_device_status.argtypes = []
@@ -181,6 +184,24 @@ def zero3_unit_gather(unit_plan: ZeroPlan, shards, full, stream=None) -> None:
         raise ZeroError(rc, "zero3_unit_gather")
 
 
+def zero3_unit_step(unit_plan: ZeroPlan, rank: int, shards, full, grads, master, m, v, param, *,
+                    lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+                    t: int, grad_layout: int = ZERO_GRAD_SHARD,
+                    param_layout: int = ZERO_PARAM_SHARD, stream=None) -> None:
+    """One ZeRO-3 unit: the gather of the `world` bf16 shards into `full` and rank
+    `rank`'s fused step, in one launch (the same results as zero3_unit_gather followed
+    by zero_adam_step; the two parts' buffers must be disjoint)."""
+    if len(shards) != unit_plan.world or len(grads) != unit_plan.world:
+        raise ValueError(f"expected {unit_plan.world} shards and gradient buffers")
+    sp = (ctypes.c_void_p * len(shards))(*[_addr(x) for x in shards])
+    gp = (ctypes.c_void_p * len(grads))(*[_addr(g) for g in grads])
+    rc = _lib.zero3_unit_step(ctypes.byref(unit_plan), rank, sp, _addr(full), gp, grad_layout,
+                              _addr(master), _addr(m), _addr(v), _addr(param), param_layout, lr,
+                              beta1, beta2, eps, t, _stream_handle(stream))
+    if rc != ZERO_OK:
+        raise ZeroError(rc, "zero3_unit_step")
+
+
 def rows_layout(shapes, world: int):
     """(elements of one rank's shard, elements of the unit) of the FSDP2-style layout."""
     return (sum(-(-r // world) * c for r, c in shapes), sum(r * c for r, c in shapes))
@@ -235,8 +256,8 @@ def raw_lib() -> ctypes.CDLL:
 
 
 __all__ = ["zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero3_unit_gather_rows", "rows_layout", "device_status", "check_device",
-           "test_withhold_copies",
+           "zero3_unit_gather_rows", "zero3_unit_step", "rows_layout", "device_status",
+           "check_device", "test_withhold_copies",
            "ZeroPlan", "ZeroError", "strerror", "version", "raw_lib", "ZERO_ALL_RANKS",
            "ZERO_GRAD_FULL", "ZERO_GRAD_SHARD", "ZERO_GRAD_WINDOW", "ZERO_GRAD_F32",
            "ZERO_ACC_BF16", "ZERO_PARAM_FULL", "ZERO_PARAM_SHARD", "ZERO_MAX_WORLD",

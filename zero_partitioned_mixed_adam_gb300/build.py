@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libzeroadam.so")
 OBJ_DIR = os.path.join(ROOT, "_build", "zeroadam")
 SOURCES = ["capi.cpp", "adam_step.cu", "unit_gather.cu"]
-HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(ROOT, "include", "zeroadam.h")]
+HEADERS = ([os.path.join(CSRC, h) for h in sorted(os.listdir(CSRC)) if h.endswith(".h")]
+           + [os.path.join(ROOT, "include", "zeroadam.h")])
 ARCH = "sm_103a"
 
 

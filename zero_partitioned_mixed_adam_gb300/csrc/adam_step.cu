@@ -12,9 +12,10 @@
 // parameter) bytes and does ~20 fp32 operations: it is bound by HBM
 // bandwidth, so it is written as a streaming kernel (16-byte vector
 // loads/stores, a persistent grid-stride loop of 512-thread blocks sized to
-// the SM count) and uses no tensor cores.  For N = 16 and N = 8 with aligned
-// buffers, TMA-staged variants (bulk copies into a shared-memory ring, one
-// CTA per SM) replace it.
+// the SM count) and uses no tensor cores.  With aligned buffers, TMA-staged
+// variants (bulk copies into a shared-memory ring, one CTA per SM) replace it:
+// gradients and state staged at N = 16, gradients staged in rank groups at
+// every other N >= 5.
 //
 // Bit-exactness: every operation is an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nvcc cannot contract any
@@ -32,6 +33,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "gather_ring.h"
 #include "internal.h"
 #include "tma_ops.h"
 
@@ -278,9 +280,9 @@ __global__ void __launch_bounds__(kThreads)
 
 // ---------------------------------------------------------------------------
 // TMA-staged variant for N = 16, bf16 gradients, fp32 sum (measured faster
-// than the register-staged kernel there; at N = 8 the state-staged ring leaves
-// room for too few consumer warps, and zero_adam_step_tma_grad_kernel below is
-// used instead).
+// than the register-staged kernel there; at other N the state-staged ring
+// leaves room for too few consumer warps, and zero_adam_step_tma_grad_kernel
+// below is used instead).
 // One CTA per SM.  Warp 0 lane 0 is the producer: for each 2048-element tile
 // it issues one bulk copy (cp.async.bulk, the TMA engine) per rank's gradient
 // tile and per state array into a two-stage shared-memory ring, and the
@@ -459,138 +461,256 @@ bool launch_tma(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* err) {
 }
 
 // ---------------------------------------------------------------------------
-// TMA-staged gradients, register-staged state: the variant for N = 8, bf16
-// gradients, fp32 sum.  One CTA per SM.  The producer lane bulk-copies only
-// the N gradient tiles of each 3072-element tile into a three-stage ring
-// (8 x 6 KB per stage).  Each of the 24 consumer warps' threads owns 4
-// elements of the tile: it loads their master, m and v straight into
-// registers before it waits for the stage, so those loads overlap the
-// gradient copies, then sums the gradients from shared memory, runs
-// adam_element and stores.  At N = 8 an element carries 42 bytes instead of
-// 58, so the arithmetic per byte is higher than at N = 16: with the state
-// staged too, only 8 consumer warps fit beside the ring and they fall behind
-// the copies; with the gradients alone, 24 do not.  Waits are bounded as in
-// the kernel above, with the same status word.
+// TMA-staged gradients, register-staged state: the variant for every other
+// N >= 5 (bf16 gradients, fp32 sum, buffers 16-byte aligned).  One CTA per SM.
+// A tile of TILE = CW*32*EPT elements is reduced over the ranks in groups of
+// G: ring stage k holds G ranks' gradient tiles (G bulk copies of TILE*2
+// bytes, cp.async.bulk on the TMA engine), so a tile passes through
+// ceil(N/G) stages and the ring depth in bytes does not grow with N.  Warp 0
+// is the producer: lane 0 arms the stage's mbarrier with its byte count, then
+// lane r issues rank r's copy, so N copies per tile go out in parallel
+// instead of from one thread.  The CW consumer warps' threads each own EPT
+// consecutive elements of the tile: they load their master, m and v into
+// registers (16- or 8-byte loads) before they wait for the first group, so
+// those loads overlap the gradient copies; they add the groups in rank order
+// from shared memory, hand each stage back, and after the last group run
+// adam_element and store.  Waits are bounded as in the kernel above, with the
+// same status word.
+//
+// Two shapes, chosen by N (measured on GB300 against the register-staged
+// kernel, bit-exact in every case): G = 8, EPT = 4, 24 consumer warps, 3
+// stages of 48 KB for 5 <= N < 40 (N = 5: 0.68 -> 0.91 of the copy peak,
+// N = 12: 0.72 -> 1.02, N = 32: 0.93 -> 0.96 on a 6.3M-element shard; equal to
+// the earlier N = 8-only kernel, which had this shape with one issuing
+// thread); G = 32, EPT = 2, 16 consumer warps, 3 stages of 64 KB for N >= 40
+// (N = 64: 0.92 -> 0.975 on a 3.16M-element shard, 0.99 -> 1.00 on 8.4M).
 
-constexpr int kTgEpt = 4;                          // elements per consumer thread
-constexpr int kTgConsumers = 768;                  // 24 warps
-constexpr int kTgTile = kTgConsumers * kTgEpt;     // 3072 elements
-constexpr int kTgStages = 3;
+template <int CAP>
+struct GradStagedArgs {
+  const uint16_t* g[CAP];  // rank k's gradient, at the range's first element
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* param;
+  int64_t n;      // elements in the range
+  int64_t nbody;  // multiple of 8: [0, nbody) through the ring, [nbody, n) scalar
+  int32_t world;
+  int32_t withhold;  // test hook: the producer issues no copies, so every wait runs out
+  AdamScalars s;
+};
 
-constexpr size_t tma_grad_smem_bytes(int nt) {
-  return static_cast<size_t>(kTgStages) * nt * kTgTile * 2;
+// EPT consecutive bf16 gradients of one rank from shared memory, added to acc.
+template <int EPT>
+__device__ __forceinline__ void add_smem_bf16(float* acc, const uint8_t* p) {
+  if constexpr (EPT == 2) {
+    const uint32_t q = *reinterpret_cast<const uint32_t*>(p);
+    acc[0] = __fadd_rn(acc[0], bf16_lo(q));
+    acc[1] = __fadd_rn(acc[1], bf16_hi(q));
+  } else if constexpr (EPT == 4) {
+    const uint2 q = *reinterpret_cast<const uint2*>(p);
+    acc[0] = __fadd_rn(acc[0], bf16_lo(q.x));
+    acc[1] = __fadd_rn(acc[1], bf16_hi(q.x));
+    acc[2] = __fadd_rn(acc[2], bf16_lo(q.y));
+    acc[3] = __fadd_rn(acc[3], bf16_hi(q.y));
+  } else {
+    accumulate_bf16x8(acc, *reinterpret_cast<const uint4*>(p));
+  }
 }
-static_assert(tma_grad_smem_bytes(8) <= 227 * 1024, "ring exceeds one CTA's shared memory");
 
-template <int NT>
-__global__ void __launch_bounds__(kTgConsumers + 32, 1)
-    zero_adam_step_tma_grad_kernel(const __grid_constant__ TmaArgs<NT> a) {
-  constexpr int64_t kGradBytes = kTgTile * 2;  // one rank's gradient tile
-  constexpr int64_t kStage = NT * kGradBytes;
+// EPT (2, 4 or 8) fp32 state values: one or two vector loads / stores.
+template <int EPT>
+__device__ __forceinline__ void load_state_vec(const float* p, float* x) {
+  if constexpr (EPT == 2) {
+    const float2 q = ld_state(reinterpret_cast<const float2*>(p));
+    x[0] = q.x;
+    x[1] = q.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPT; j += 4) {
+      const float4 q = ld_state(reinterpret_cast<const float4*>(p + j));
+      x[j] = q.x;
+      x[j + 1] = q.y;
+      x[j + 2] = q.z;
+      x[j + 3] = q.w;
+    }
+  }
+}
+template <int EPT>
+__device__ __forceinline__ void store_state_vec(float* p, const float* x) {
+  if constexpr (EPT == 2) {
+    __stcs(reinterpret_cast<float2*>(p), make_float2(x[0], x[1]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPT; j += 4)
+      __stcs(reinterpret_cast<float4*>(p + j), make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]));
+  }
+}
+template <int EPT>
+__device__ __forceinline__ void store_param_vec(uint16_t* p, const float* x) {
+  if constexpr (EPT == 2) {
+    __stcs(reinterpret_cast<unsigned int*>(p), pack_bf16x2_rn(x[0], x[1]));
+  } else if constexpr (EPT == 4) {
+    __stcs(reinterpret_cast<uint2*>(p),
+           make_uint2(pack_bf16x2_rn(x[0], x[1]), pack_bf16x2_rn(x[2], x[3])));
+  } else {
+    store_bf16x8_rn(p, true, x);
+  }
+}
+
+template <int G, int EPT, int CW, int STAGES>
+struct GradStagedShape {
+  static constexpr int kTile = CW * 32 * EPT;            // elements per tile
+  static constexpr int64_t kGradBytes = int64_t{kTile} * 2;  // one rank's tile
+  static constexpr int64_t kStage = G * kGradBytes;      // one stage: G ranks
+  static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage;
+  static_assert(G >= 1 && G <= 32, "one producer lane per rank of a group");
+  static_assert(EPT == 2 || EPT == 4 || EPT == 8, "2, 4 or 8 elements per thread");
+  static_assert(kTile % 8 == 0, "tiles start on 16-byte boundaries");
+  static_assert(kSmem <= 227 * 1024, "ring exceeds one CTA's shared memory");
+};
+
+// The producer warp of the gradient-staged step (all 32 lanes).
+template <int G, int EPT, int CW, int STAGES, int CAP>
+__device__ void grad_stage_producer(const GradStagedArgs<CAP>& a, uint8_t* ring, uint64_t* full,
+                                    uint64_t* empty, int lane) {
+  using Shape = GradStagedShape<G, EPT, CW, STAGES>;
+  constexpr int kTile = Shape::kTile;
+  const int world = a.world;
+  const int ngroups = (world + G - 1) / G;
+  const int64_t ntiles = (a.nbody + kTile - 1) / kTile;
+  int64_t k = 0;  // stages issued
+  bool ok = true;
+  for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+    const int64_t e0 = tile * kTile;
+    int64_t cnt = a.nbody - e0;
+    if (cnt > kTile) cnt = kTile;
+    const uint32_t gbytes = static_cast<uint32_t>(cnt * 2);  // a multiple of 16
+    for (int grp = 0; grp < ngroups; ++grp) {
+      const int s = static_cast<int>(k % STAGES);
+      if (k >= STAGES) {
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(&empty[s], static_cast<uint32_t>((k / STAGES - 1) & 1)) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!a.withhold) {
+        const int r0 = grp * G;
+        const int nr = world - r0 < G ? world - r0 : G;
+        uint8_t* st = ring + s * Shape::kStage;
+        if (lane == 0) mbar_expect_tx(&full[s], gbytes * nr);
+        __syncwarp();
+        if (lane < nr)
+          bulk_load(st + lane * Shape::kGradBytes, a.g[r0 + lane] + e0, gbytes, &full[s]);
+      }
+      ++k;
+    }
+  }
+  if (!ok && lane == 0) {
+    atomicExch(&g_step_status, 1);
+    const int64_t first = k > STAGES ? k - STAGES : 0;
+    for (int64_t j = first; j < k && !a.withhold; ++j)
+      mbar_wait(&full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1));
+  }
+}
+
+// The consumer warps of the gradient-staged step; t = thread index among them.
+// False if a wait gave up (the step is incomplete; nothing more is written).
+template <int G, int EPT, int CW, int STAGES, int CAP>
+__device__ bool grad_stage_consumer(const GradStagedArgs<CAP>& a, const uint8_t* ring,
+                                    uint64_t* full, uint64_t* empty, int t, int lane) {
+  using Shape = GradStagedShape<G, EPT, CW, STAGES>;
+  constexpr int kTile = Shape::kTile;
+  const int world = a.world;
+  const int ngroups = (world + G - 1) / G;
+  const int64_t ntiles = (a.nbody + kTile - 1) / kTile;
+  int64_t k = 0;  // stages consumed
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t e0 = tile * kTile + static_cast<int64_t>(EPT) * t;
+    const bool in = e0 < a.nbody;  // e0 a multiple of EPT, nbody of 8: all EPT are in
+    float acc[EPT], w[EPT], mm[EPT], vv[EPT];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      acc[j] = -0.0f;
+      w[j] = mm[j] = vv[j] = 0.0f;
+    }
+    if (in) {
+      load_state_vec<EPT>(a.master + e0, w);
+      load_state_vec<EPT>(a.m + e0, mm);
+      load_state_vec<EPT>(a.v + e0, vv);
+    }
+    for (int grp = 0; grp < ngroups; ++grp, ++k) {
+      const int s = static_cast<int>(k % STAGES);
+      if (!mbar_wait(&full[s], static_cast<uint32_t>((k / STAGES) & 1))) {
+        atomicExch(&g_step_status, 2);
+        return false;
+      }
+      const int nr = world - grp * G < G ? world - grp * G : G;
+      const uint8_t* st = ring + s * Shape::kStage + 2 * EPT * t;
+      if (in) {
+#pragma unroll
+        for (int r = 0; r < G; ++r)
+          if (r < nr) add_smem_bf16<EPT>(acc, st + r * Shape::kGradBytes);
+      }
+      // every lane has read its slice of stage s: the warp hands the stage back
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (in) {
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) adam_element(acc[j], a.s, w[j], mm[j], vv[j]);
+      store_state_vec<EPT>(a.master + e0, w);
+      store_state_vec<EPT>(a.m + e0, mm);
+      store_state_vec<EPT>(a.v + e0, vv);
+      store_param_vec<EPT>(a.param + e0, w);
+    }
+  }
+  return true;
+}
+
+// The last few (< 8) elements of a staged range, one per thread t of block 0.
+template <int CAP>
+__device__ void staged_tail(const GradStagedArgs<CAP>& a, int t) {
+  if (blockIdx.x != 0 || a.nbody + t >= a.n) return;
+  const int64_t e = a.nbody + t;
+  float acc = -0.0f;
+  for (int r = 0; r < a.world; ++r) acc = __fadd_rn(acc, bf16_to_f32(ld_grad(a.g[r] + e)));
+  float w = ld_state(a.master + e), mm = ld_state(a.m + e), vv = ld_state(a.v + e);
+  adam_element(acc, a.s, w, mm, vv);
+  a.master[e] = w;
+  a.m[e] = mm;
+  a.v[e] = vv;
+  a.param[e] = f32_to_bf16_rn(w);
+}
+
+template <int G, int EPT, int CW, int STAGES, int CAP>
+__global__ void __launch_bounds__(CW * 32 + 32, 1)
+    zero_adam_step_tma_grad_kernel(const __grid_constant__ GradStagedArgs<CAP> a) {
   extern __shared__ __align__(1024) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[kTgStages], empty[kTgStages];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t ntiles = (a.nbody + kTgTile - 1) / kTgTile;
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTgStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kTgConsumers / 32);
+      mbar_init(&empty[s], CW);
     }
     mbar_init_fence();
   }
   __syncthreads();
-
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (warp == 0) {
-    if (lane != 0) return;
-    int64_t k = 0;
-    bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
-      const int s = static_cast<int>(k % kTgStages);
-      if (k >= kTgStages &&
-          !mbar_wait(&empty[s], static_cast<uint32_t>((k / kTgStages - 1) & 1))) {
-        ok = false;
-        break;
-      }
-      if (a.withhold) continue;
-      const int64_t e0 = tile * kTgTile;
-      int64_t cnt = a.nbody - e0;
-      if (cnt > kTgTile) cnt = kTgTile;
-      const uint32_t gbytes = static_cast<uint32_t>(cnt * 2);  // a multiple of 16
-      uint8_t* st = ring + s * kStage;
-      mbar_expect_tx(&full[s], gbytes * NT);
-      for (int r = 0; r < NT; ++r) bulk_load(st + r * kGradBytes, a.g[r] + e0, gbytes, &full[s]);
-    }
-    if (!ok) {
-      atomicExch(&g_step_status, 1);
-      const int64_t first = k > kTgStages ? k - kTgStages : 0;
-      for (int64_t j = first; j < k && !a.withhold; ++j)
-        mbar_wait(&full[j % kTgStages], static_cast<uint32_t>((j / kTgStages) & 1));
-    }
+    grad_stage_producer<G, EPT, CW, STAGES, CAP>(a, ring, full, empty, lane);
     return;
   }
-
   const int t = threadIdx.x - 32;
-  int64_t k = 0;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
-    const int s = static_cast<int>(k % kTgStages);
-    const int64_t e0 = tile * kTgTile + kTgEpt * t;
-    const bool in = e0 < a.nbody;  // e0 is a multiple of 4, nbody of 8: all 4 are in
-    float4 w = make_float4(0.f, 0.f, 0.f, 0.f), mm = w, vv = w;
-    if (in) {
-      w = ld_state(reinterpret_cast<const float4*>(a.master + e0));
-      mm = ld_state(reinterpret_cast<const float4*>(a.m + e0));
-      vv = ld_state(reinterpret_cast<const float4*>(a.v + e0));
-    }
-    if (!mbar_wait(&full[s], static_cast<uint32_t>((k / kTgStages) & 1))) {
-      atomicExch(&g_step_status, 2);
-      return;
-    }
-    const uint8_t* st = ring + s * kStage;
-    float acc[4] = {-0.0f, -0.0f, -0.0f, -0.0f};
-    if (in) {
-#pragma unroll
-      for (int r = 0; r < NT; ++r) {
-        const uint2 q = *reinterpret_cast<const uint2*>(st + r * kGradBytes + 2 * kTgEpt * t);
-        acc[0] = __fadd_rn(acc[0], bf16_lo(q.x));
-        acc[1] = __fadd_rn(acc[1], bf16_hi(q.x));
-        acc[2] = __fadd_rn(acc[2], bf16_lo(q.y));
-        acc[3] = __fadd_rn(acc[3], bf16_hi(q.y));
-      }
-    }
-    // every lane has read its slice of stage s: the warp hands the stage back
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (in) {
-      adam_element(acc[0], a.s, w.x, mm.x, vv.x);
-      adam_element(acc[1], a.s, w.y, mm.y, vv.y);
-      adam_element(acc[2], a.s, w.z, mm.z, vv.z);
-      adam_element(acc[3], a.s, w.w, mm.w, vv.w);
-      __stcs(reinterpret_cast<float4*>(a.master + e0), w);
-      __stcs(reinterpret_cast<float4*>(a.m + e0), mm);
-      __stcs(reinterpret_cast<float4*>(a.v + e0), vv);
-      __stcs(reinterpret_cast<uint2*>(a.param + e0),
-             make_uint2(pack_bf16x2_rn(w.x, w.y), pack_bf16x2_rn(w.z, w.w)));
-    }
-  }
-  // the last few (< 8) elements of the range, one per thread of block 0
-  if (blockIdx.x == 0 && a.nbody + t < a.n) {
-    const int64_t e = a.nbody + t;
-    float acc = -0.0f;
-#pragma unroll
-    for (int r = 0; r < NT; ++r) acc = __fadd_rn(acc, bf16_to_f32(ld_grad(a.g[r] + e)));
-    float w = ld_state(a.master + e), mm = ld_state(a.m + e), vv = ld_state(a.v + e);
-    adam_element(acc, a.s, w, mm, vv);
-    a.master[e] = w;
-    a.m[e] = mm;
-    a.v[e] = vv;
-    a.param[e] = f32_to_bf16_rn(w);
-  }
+  if (grad_stage_consumer<G, EPT, CW, STAGES, CAP>(a, ring, full, empty, t, lane))
+    staged_tail(a, t);
 }
 
-// As launch_tma, for the gradient-staged kernel.
-template <int NT>
-bool launch_tma_grad(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* err) {
-  if (!(a.head == 0 && a.gvec && a.svec && a.pvec) || a.nvec < 1) return false;
+template <int G, int EPT, int CW, int STAGES, int CAP>
+bool launch_tma_grad_shape(const StepLaunch& L, int64_t nbody, cudaError_t* err) {
+  using Shape = GradStagedShape<G, EPT, CW, STAGES>;
   static std::mutex mu;
   static bool configured[64] = {false};
   int dev = 0;
@@ -598,9 +718,9 @@ bool launch_tma_grad(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* er
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured[dev]) {
-      if (cudaFuncSetAttribute(zero_adam_step_tma_grad_kernel<NT>,
+      if (cudaFuncSetAttribute(zero_adam_step_tma_grad_kernel<G, EPT, CW, STAGES, CAP>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tma_grad_smem_bytes(NT))) != cudaSuccess) {
+                               static_cast<int>(Shape::kSmem)) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
       }
@@ -609,20 +729,203 @@ bool launch_tma_grad(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* er
   }
   int sms = 0;
   if (device_sm_count(&sms) != 0) return false;
-  TmaArgs<NT> t;
-  for (int k = 0; k < NT; ++k) t.g[k] = static_cast<const uint16_t*>(L.grads[k]);
+  GradStagedArgs<CAP> t;
+  for (int k = 0; k < L.world; ++k) t.g[k] = static_cast<const uint16_t*>(L.grads[k]);
+  for (int k = L.world; k < CAP; ++k) t.g[k] = nullptr;
   t.master = L.master;
   t.m = L.m;
   t.v = L.v;
   t.param = L.param;
   t.n = L.n;
-  t.nbody = 8 * a.nvec;
+  t.nbody = nbody;
+  t.world = L.world;
   t.withhold = L.withhold;
   t.s = L.s;
-  const int64_t ntiles = (t.nbody + kTgTile - 1) / kTgTile;
+  const int64_t ntiles = (nbody + Shape::kTile - 1) / Shape::kTile;
   const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
-  zero_adam_step_tma_grad_kernel<NT>
-      <<<grid, kTgConsumers + 32, tma_grad_smem_bytes(NT), L.stream>>>(t);
+  zero_adam_step_tma_grad_kernel<G, EPT, CW, STAGES, CAP>
+      <<<grid, CW * 32 + 32, Shape::kSmem, L.stream>>>(t);
+  *err = cudaGetLastError();
+  return true;
+}
+
+// The gradient-staged kernel for N >= 5 (not 16), when every buffer is
+// 16-byte aligned at the range's first element.  Returns false when it does
+// not apply.
+bool launch_tma_grad(const StepLaunch& L, int32_t head, int64_t nvec, bool all_vec,
+                     cudaError_t* err) {
+  if (!(head == 0 && all_vec) || nvec < 1 || L.world < 5 || L.world == 16) return false;
+  const int64_t nbody = 8 * nvec;
+  if (L.world < 40) return launch_tma_grad_shape<8, 4, 24, 3, 64>(L, nbody, err);
+  if (L.world <= 64) return launch_tma_grad_shape<32, 2, 16, 3, 64>(L, nbody, err);
+  return launch_tma_grad_shape<32, 2, 16, 3, kTableRuntime>(L, nbody, err);
+}
+
+// ---------------------------------------------------------------------------
+// ZeRO-3 unit step ("ZeRO and FSDP" -> "ZeRO-3 and FSDP"): the unit's
+// all-gather of the N bf16 parameter shards and one rank's fused step on its
+// shard, in one launch.  The step never reads the gathered unit and the
+// gather never reads what the step writes (the host checks that the buffers
+// are disjoint), so the two can run side by side: every CTA (one per SM) runs
+// the gather's TMA copy ring in warp 1 (its chunks blockIdx.x + i*gridDim.x)
+// beside its share of the step's tiles (warp 0 the gradient producer, the CW
+// warps from 2 on the consumers).  Each part pays no launch of its own, and a
+// small unit's gather and step overlap their ramps and DRAM round trips
+// instead of running one after the other.  For N <= 4 the consumers read the
+// gradients straight from global memory (GREG: no gradient ring; at small N
+// the register-staged form measured faster).  Results are bit for bit those
+// of zero3_unit_gather followed by zero_adam_step.
+
+template <int CAP>
+struct FlatGatherPart {
+  const uint16_t* src[CAP];  // the N parameter shards
+  uint16_t* full;
+  int64_t numel;
+  int64_t u8;     // numel rounded down to a multiple of 8: [0, u8) moves by TMA
+  int64_t shard;  // a multiple of 8
+};
+
+template <int CAP>
+struct UnitStepArgs {
+  GradStagedArgs<CAP> step;
+  FlatGatherPart<CAP> gather;
+};
+
+// Register-staged consumers for the fused kernel at N <= 4: tiles of
+// CW*32*EPT elements, each thread loads its EPT gradients of every rank and
+// its state, sums in rank order, updates and stores.
+template <int EPT, int CW, int CAP>
+__device__ void grad_reg_consumer(const GradStagedArgs<CAP>& a, int t) {
+  constexpr int kTile = CW * 32 * EPT;
+  static_assert(EPT == 8, "one 16-byte gradient load per rank");
+  const int64_t ntiles = (a.nbody + kTile - 1) / kTile;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t e0 = tile * kTile + static_cast<int64_t>(EPT) * t;
+    if (e0 >= a.nbody) continue;
+    uint4 r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (k < a.world) r[k] = ld_grad(reinterpret_cast<const uint4*>(a.g[k] + e0));
+    float w[8], mm[8], vv[8], acc[8];
+    load_state_vec<8>(a.master + e0, w);
+    load_state_vec<8>(a.m + e0, mm);
+    load_state_vec<8>(a.v + e0, vv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = -0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (k < a.world) accumulate_bf16x8(acc, r[k]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adam_element(acc[j], a.s, w[j], mm[j], vv[j]);
+    store_state_vec<8>(a.master + e0, w);
+    store_state_vec<8>(a.m + e0, mm);
+    store_state_vec<8>(a.v + e0, vv);
+    store_param_vec<8>(a.param + e0, w);
+  }
+}
+
+template <int G, int EPT, int CW, int STAGES, int SLOTS, int CAP, bool GREG>
+struct UnitStepShape {
+  using Step = GradStagedShape<G, EPT, CW, STAGES>;
+  static constexpr size_t kStepRing = GREG ? 0 : Step::kSmem;
+  static constexpr size_t kSmem = kStepRing + static_cast<size_t>(SLOTS) * kSlotBytes;
+  static_assert(kSmem + 1024 <= 227 * 1024, "rings exceed one CTA's shared memory");
+};
+
+template <int G, int EPT, int CW, int STAGES, int SLOTS, int CAP, bool GREG>
+__global__ void __launch_bounds__(CW * 32 + 64, 1)
+    zero3_unit_step_kernel(const __grid_constant__ UnitStepArgs<CAP> a) {
+  using Shape = UnitStepShape<G, EPT, CW, STAGES, SLOTS, CAP, GREG>;
+  extern __shared__ __align__(1024) uint8_t ring[];  // [step ring][gather ring]
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], gbar[SLOTS];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], CW);
+    }
+    for (int s = 0; s < SLOTS; ++s) mbar_init(&gbar[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    if (!GREG) grad_stage_producer<G, EPT, CW, STAGES, CAP>(a.step, ring, full, empty, lane);
+    return;
+  }
+  if (warp == 1) {
+    const FlatGatherPart<CAP>& g = a.gather;
+    // the unit's last (< 8) elements, lanes of block 0
+    if (blockIdx.x == 0 && g.u8 + lane < g.numel && !a.step.withhold) {
+      const int64_t e = g.u8 + lane;
+      const int64_t r = e / g.shard;
+      g.full[e] = g.src[r][e - r * g.shard];
+    }
+    const int64_t nchunks = flat_chunks(g.u8);
+    if (lane != 0 || blockIdx.x >= nchunks) return;
+    const int64_t mine = (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    FlatLayout<FlatGatherPart<CAP>> layout{g};
+    ring_copy<SLOTS>(layout, mine, ring + Shape::kStepRing, gbar, a.step.withhold != 0,
+                     &g_step_status);
+    return;
+  }
+  const int t = threadIdx.x - 64;
+  if constexpr (GREG) {
+    grad_reg_consumer<EPT, CW, CAP>(a.step, t);
+    staged_tail(a.step, t);
+  } else {
+    if (grad_stage_consumer<G, EPT, CW, STAGES, CAP>(a.step, ring, full, empty, t, lane))
+      staged_tail(a.step, t);
+  }
+}
+
+template <int G, int EPT, int CW, int STAGES, int SLOTS, int CAP, bool GREG>
+bool launch_unit_step_shape(const GatherLaunch& GL, const StepLaunch& L, int64_t nbody,
+                            cudaError_t* err) {
+  using Shape = UnitStepShape<G, EPT, CW, STAGES, SLOTS, CAP, GREG>;
+  auto kernel = zero3_unit_step_kernel<G, EPT, CW, STAGES, SLOTS, CAP, GREG>;
+  static std::mutex mu;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Shape::kSmem)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+      }
+      configured[dev] = true;
+    }
+  }
+  int sms = 0;
+  if (device_sm_count(&sms) != 0) return false;
+  UnitStepArgs<CAP> u;
+  GradStagedArgs<CAP>& t = u.step;
+  for (int k = 0; k < L.world; ++k) t.g[k] = static_cast<const uint16_t*>(L.grads[k]);
+  for (int k = L.world; k < CAP; ++k) t.g[k] = nullptr;
+  t.master = L.master;
+  t.m = L.m;
+  t.v = L.v;
+  t.param = L.param;
+  t.n = L.n;
+  t.nbody = nbody;
+  t.world = L.world;
+  t.withhold = L.withhold;
+  t.s = L.s;
+  FlatGatherPart<CAP>& g = u.gather;
+  for (int k = 0; k < GL.world; ++k) g.src[k] = GL.shards[k];
+  for (int k = GL.world; k < CAP; ++k) g.src[k] = nullptr;
+  g.full = GL.full;
+  g.numel = GL.numel;
+  g.u8 = GL.numel & ~static_cast<int64_t>(7);
+  g.shard = GL.shard;
+  constexpr int64_t kTile = GREG ? int64_t{CW} * 32 * EPT : Shape::Step::kTile;
+  int64_t work = (nbody + kTile - 1) / kTile;
+  const int64_t nchunks = flat_chunks(g.u8);
+  if (nchunks > work) work = nchunks;
+  const int grid = static_cast<int>(work < sms ? (work < 1 ? 1 : work) : sms);
+  kernel<<<grid, CW * 32 + 64, Shape::kSmem, L.stream>>>(u);
   *err = cudaGetLastError();
   return true;
 }
@@ -695,9 +998,9 @@ cudaError_t launch_world(const StepLaunch& L) {
     cudaError_t err = cudaSuccess;
     if (launch_tma<16>(L, a, &err)) return err;
   }
-  if constexpr (NT == 8 && CAP == 8 && !GF32 && !ABF16) {
+  if constexpr (!GF32 && !ABF16) {
     cudaError_t err = cudaSuccess;
-    if (launch_tma_grad<8>(L, a, &err)) return err;
+    if (launch_tma_grad(L, a.head, a.nvec, a.gvec && a.svec && a.pvec, &err)) return err;
   }
 
   const void* kern = reinterpret_cast<const void*>(&zero_adam_step_kernel<NT, CAP, GF32, ABF16>);
@@ -726,7 +1029,34 @@ cudaError_t launch_variant(const StepLaunch& L) {
   }
 }
 
+// The fused unit step when both parts can run on the TMA engine: the gather's
+// shard a multiple of 8 elements, and every buffer of both parts 16-byte
+// aligned at its first element; bf16 gradients, fp32 sum.
+bool launch_unit_step_fused(const GatherLaunch& GL, const StepLaunch& L, cudaError_t* err) {
+  if (L.grad_f32 || L.acc_bf16 || L.n < 8 || GL.numel < 8 || GL.shard % 8 != 0) return false;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  bool ok = a16(GL.full) && a16(L.master) && a16(L.m) && a16(L.v) && a16(L.param);
+  for (int k = 0; k < GL.world && ok; ++k) ok = a16(GL.shards[k]);
+  for (int k = 0; k < L.world && ok; ++k) ok = a16(L.grads[k]);
+  if (!ok) return false;
+  const int64_t nbody = L.n & ~static_cast<int64_t>(7);
+  if (L.world <= 4) return launch_unit_step_shape<1, 8, 24, 1, 4, 64, true>(GL, L, nbody, err);
+  if (L.world < 40) return launch_unit_step_shape<8, 4, 24, 3, 4, 64, false>(GL, L, nbody, err);
+  if (L.world <= 64) return launch_unit_step_shape<32, 2, 16, 3, 2, 64, false>(GL, L, nbody, err);
+  return launch_unit_step_shape<32, 2, 16, 3, 2, kTableRuntime, false>(GL, L, nbody, err);
+}
+
 }  // namespace
+
+cudaError_t launch_unit_step(const GatherLaunch& GL, const StepLaunch& L) {
+  (void)cudaGetLastError();  // launch errors below are this call's own
+  if (L.n <= 0) return launch_unit_gather(GL);
+  cudaError_t err = cudaSuccess;
+  if (launch_unit_step_fused(GL, L, &err)) return err;
+  err = launch_unit_gather(GL);
+  if (err != cudaSuccess) return err;
+  return launch_adam_step(L);
+}
 
 namespace {
 __device__ int g_step_status_taken;

@@ -133,11 +133,20 @@ Range bytes_of(const void* p, int64_t first, int64_t count, int esize) {
   return {b, b + static_cast<uintptr_t>(count) * esize};
 }
 
-// The checks and the launch of one step over [begin, end) (both entry points).
-int step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end,
-               const void* const* grad_ptrs, int32_t grad_layout, float* master, float* m,
-               float* v, void* param_bf16, int32_t param_layout, double lr, double beta1,
-               double beta2, double eps, int64_t t, void* stream) {
+// A step over [begin, end), checked: its launch and the byte ranges it
+// touches (for the unit step's checks across its two parts).
+struct PreparedStep {
+  StepLaunch L;
+  const void* g[ZERO_MAX_WORLD];    // gradient pointers at the range's first element
+  Range outs[4];                    // master, m, v, param bytes written (L.n > 0)
+  Range grads[ZERO_MAX_WORLD];      // gradient bytes read (L.n > 0)
+};
+
+// The checks of one step over [begin, end) (every step entry point).
+int prepare_step(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end,
+                 const void* const* grad_ptrs, int32_t grad_layout, float* master, float* m,
+                 float* v, void* param_bf16, int32_t param_layout, double lr, double beta1,
+                 double beta2, double eps, int64_t t, void* stream, PreparedStep* ps) {
   int rc = check_plan(plan);
   if (rc != ZERO_OK) return rc;
   const int32_t N = static_cast<int32_t>(plan->world);
@@ -190,26 +199,26 @@ int step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end
     if (misaligned(grad_ptrs[k], gsize)) return ZERO_E_ALIGN;
 
   if (n > 0) {
-    const Range outs[4] = {bytes_of(master, s_first, n, 4), bytes_of(m, s_first, n, 4),
-                           bytes_of(v, s_first, n, 4), bytes_of(param_bf16, p_first, n, 2)};
+    ps->outs[0] = bytes_of(master, s_first, n, 4);
+    ps->outs[1] = bytes_of(m, s_first, n, 4);
+    ps->outs[2] = bytes_of(v, s_first, n, 4);
+    ps->outs[3] = bytes_of(param_bf16, p_first, n, 2);
     for (int i = 0; i < 4; ++i)
       for (int j = i + 1; j < 4; ++j)
-        if (overlap(outs[i], outs[j])) return ZERO_E_ALIAS;
+        if (overlap(ps->outs[i], ps->outs[j])) return ZERO_E_ALIAS;
     for (int32_t k = 0; k < N; ++k) {
-      const Range g = bytes_of(grad_ptrs[k], g_first, n, gsize);
+      ps->grads[k] = bytes_of(grad_ptrs[k], g_first, n, gsize);
       for (int i = 0; i < 4; ++i)
-        if (overlap(g, outs[i])) return ZERO_E_ALIAS;
+        if (overlap(ps->grads[k], ps->outs[i])) return ZERO_E_ALIAS;
     }
   }
-  if (n == 0) return ZERO_OK;
 
   // Offset every pointer to the range's first element.
-  const void* g[ZERO_MAX_WORLD];
   for (int32_t k = 0; k < N; ++k)
-    g[k] = static_cast<const char*>(grad_ptrs[k]) + g_first * gsize;
+    ps->g[k] = static_cast<const char*>(grad_ptrs[k]) + g_first * gsize;
 
-  StepLaunch L;
-  L.grads = g;
+  StepLaunch& L = ps->L;
+  L.grads = ps->g;
   L.world = N;
   L.grad_f32 = (gflags & ZERO_GRAD_F32) ? 1 : 0;
   L.acc_bf16 = (gflags & ZERO_ACC_BF16) ? 1 : 0;
@@ -220,20 +229,59 @@ int step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t end
   L.n = n;
   L.stream = static_cast<cudaStream_t>(stream);
   L.withhold = g_withhold.load(std::memory_order_relaxed);
-  AdamScalars& s = L.s;
-  s.b1 = static_cast<float>(beta1);
-  s.omb1 = static_cast<float>(1.0 - beta1);
-  s.b2 = static_cast<float>(beta2);
-  s.omb2 = static_cast<float>(1.0 - beta2);
-  s.bc1 = static_cast<float>(1.0 - std::pow(beta1, static_cast<double>(t)));
-  s.bc2 = static_cast<float>(1.0 - std::pow(beta2, static_cast<double>(t)));
-  s.lr = static_cast<float>(lr);
-  s.eps = static_cast<float>(eps);
-  s.world = static_cast<float>(N);
-  s.pow2_world = (N & (N - 1)) == 0 ? 1 : 0;
-  s.inv_world = static_cast<float>(1.0 / static_cast<double>(N));
-  return launch_status(launch_adam_step(L));
+  AdamScalars& sc = L.s;
+  sc.b1 = static_cast<float>(beta1);
+  sc.omb1 = static_cast<float>(1.0 - beta1);
+  sc.b2 = static_cast<float>(beta2);
+  sc.omb2 = static_cast<float>(1.0 - beta2);
+  sc.bc1 = static_cast<float>(1.0 - std::pow(beta1, static_cast<double>(t)));
+  sc.bc2 = static_cast<float>(1.0 - std::pow(beta2, static_cast<double>(t)));
+  sc.lr = static_cast<float>(lr);
+  sc.eps = static_cast<float>(eps);
+  sc.world = static_cast<float>(N);
+  sc.pow2_world = (N & (N - 1)) == 0 ? 1 : 0;
+  sc.inv_world = static_cast<float>(1.0 / static_cast<double>(N));
+  return ZERO_OK;
 }
+
+// A flat unit gather, checked: its launch and the byte ranges it touches.
+struct PreparedGather {
+  GatherLaunch L;
+  Range out;                         // the unit's bytes written
+  Range shards[ZERO_MAX_WORLD];      // the shards' bytes read
+};
+
+int prepare_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs, void* full_bf16,
+                   void* stream, PreparedGather* pg) {
+  int rc = check_plan(unit_plan);
+  if (rc != ZERO_OK) return rc;
+  const int32_t N = static_cast<int32_t>(unit_plan->world);
+  if (shard_ptrs == nullptr || full_bf16 == nullptr) return ZERO_E_NULLPTR;
+  for (int32_t k = 0; k < N; ++k)
+    if (shard_ptrs[k] == nullptr) return ZERO_E_NULLPTR;
+  if (reinterpret_cast<uintptr_t>(full_bf16) & 1u) return ZERO_E_ALIGN;
+  for (int32_t k = 0; k < N; ++k)
+    if (reinterpret_cast<uintptr_t>(shard_ptrs[k]) & 1u) return ZERO_E_ALIGN;
+  pg->out = bytes_of(full_bf16, 0, unit_plan->numel, 2);
+  for (int32_t k = 0; k < N; ++k) {
+    int64_t cnt = unit_plan->numel - static_cast<int64_t>(k) * unit_plan->shard;
+    if (cnt > unit_plan->shard) cnt = unit_plan->shard;
+    if (cnt < 0) cnt = 0;
+    pg->shards[k] = bytes_of(shard_ptrs[k], 0, cnt, 2);
+    if (cnt > 0 && overlap(pg->out, pg->shards[k])) return ZERO_E_ALIAS;
+  }
+  GatherLaunch& L = pg->L;
+  L.shards = reinterpret_cast<const uint16_t* const*>(shard_ptrs);
+  L.world = N;
+  L.full = static_cast<uint16_t*>(full_bf16);
+  L.numel = unit_plan->numel;
+  L.shard = unit_plan->shard;
+  L.stream = static_cast<cudaStream_t>(stream);
+  L.withhold = g_withhold.load(std::memory_order_relaxed);
+  return ZERO_OK;
+}
+
+bool nonempty(Range r) { return r.hi > r.lo; }
 
 }  // namespace
 }  // namespace zeroadam
@@ -252,8 +300,11 @@ int zero_adam_step_range(const zero_plan_t* plan, int32_t rank, int64_t begin, i
                          float* m, float* v, void* param_bf16, int32_t param_layout, double lr,
                          double beta1, double beta2, double eps, int64_t t, void* stream) {
   Trace trace("zero_adam_step_range");
-  return step_range(plan, rank, begin, end, grad_ptrs, grad_layout, master, m, v, param_bf16,
-                    param_layout, lr, beta1, beta2, eps, t, stream);
+  PreparedStep ps;
+  const int rc = prepare_step(plan, rank, begin, end, grad_ptrs, grad_layout, master, m, v,
+                              param_bf16, param_layout, lr, beta1, beta2, eps, t, stream, &ps);
+  if (rc != ZERO_OK || ps.L.n == 0) return rc;
+  return launch_status(launch_adam_step(ps.L));
 }
 
 int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* grad_ptrs,
@@ -262,8 +313,39 @@ int zero_adam_step(const zero_plan_t* plan, int32_t rank, const void* const* gra
                    int64_t t, void* stream) {
   Trace trace("zero_adam_step");
   if ((grad_layout & ZERO_GRAD_LAYOUT_MASK) == ZERO_GRAD_WINDOW) return ZERO_E_LAYOUT;
-  return step_range(plan, rank, 0, INT64_MAX, grad_ptrs, grad_layout, master, m, v, param_bf16,
-                    param_layout, lr, beta1, beta2, eps, t, stream);
+  PreparedStep ps;
+  const int rc = prepare_step(plan, rank, 0, INT64_MAX, grad_ptrs, grad_layout, master, m, v,
+                              param_bf16, param_layout, lr, beta1, beta2, eps, t, stream, &ps);
+  if (rc != ZERO_OK || ps.L.n == 0) return rc;
+  return launch_status(launch_adam_step(ps.L));
+}
+
+int zero3_unit_step(const zero_plan_t* unit_plan, int32_t rank, const void* const* shard_ptrs,
+                    void* full_bf16, const void* const* grad_ptrs, int32_t grad_layout,
+                    float* master, float* m, float* v, void* param_bf16, int32_t param_layout,
+                    double lr, double beta1, double beta2, double eps, int64_t t, void* stream) {
+  Trace trace("zero3_unit_step");
+  if ((grad_layout & ZERO_GRAD_LAYOUT_MASK) == ZERO_GRAD_WINDOW) return ZERO_E_LAYOUT;
+  PreparedGather pg;
+  int rc = prepare_gather(unit_plan, shard_ptrs, full_bf16, stream, &pg);
+  if (rc != ZERO_OK) return rc;
+  PreparedStep ps;
+  rc = prepare_step(unit_plan, rank, 0, INT64_MAX, grad_ptrs, grad_layout, master, m, v,
+                    param_bf16, param_layout, lr, beta1, beta2, eps, t, stream, &ps);
+  if (rc != ZERO_OK) return rc;
+  // The two parts run side by side: the gathered unit must not overlap what
+  // the step reads or writes, and the shards must not overlap what it writes.
+  if (ps.L.n > 0) {
+    const int32_t N = static_cast<int32_t>(unit_plan->world);
+    for (int i = 0; i < 4; ++i) {
+      if (overlap(pg.out, ps.outs[i])) return ZERO_E_ALIAS;
+      for (int32_t k = 0; k < N; ++k)
+        if (nonempty(pg.shards[k]) && overlap(pg.shards[k], ps.outs[i])) return ZERO_E_ALIAS;
+    }
+    for (int32_t k = 0; k < N; ++k)
+      if (overlap(pg.out, ps.grads[k])) return ZERO_E_ALIAS;
+  }
+  return launch_status(launch_unit_step(pg.L, ps.L));
 }
 
 int zero_test_withhold_copies(int on) {
@@ -275,30 +357,10 @@ int zero_test_withhold_copies(int on) {
 int zero3_unit_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs,
                       void* full_bf16, void* stream) {
   Trace trace("zero3_unit_gather");
-  int rc = check_plan(unit_plan);
+  PreparedGather pg;
+  const int rc = prepare_gather(unit_plan, shard_ptrs, full_bf16, stream, &pg);
   if (rc != ZERO_OK) return rc;
-  const int32_t N = static_cast<int32_t>(unit_plan->world);
-  if (shard_ptrs == nullptr || full_bf16 == nullptr) return ZERO_E_NULLPTR;
-  for (int32_t k = 0; k < N; ++k)
-    if (shard_ptrs[k] == nullptr) return ZERO_E_NULLPTR;
-  if (reinterpret_cast<uintptr_t>(full_bf16) & 1u) return ZERO_E_ALIGN;
-  for (int32_t k = 0; k < N; ++k)
-    if (reinterpret_cast<uintptr_t>(shard_ptrs[k]) & 1u) return ZERO_E_ALIGN;
-  const Range out = bytes_of(full_bf16, 0, unit_plan->numel, 2);
-  for (int32_t k = 0; k < N; ++k) {
-    int64_t cnt = unit_plan->numel - static_cast<int64_t>(k) * unit_plan->shard;
-    if (cnt > unit_plan->shard) cnt = unit_plan->shard;
-    if (cnt > 0 && overlap(out, bytes_of(shard_ptrs[k], 0, cnt, 2))) return ZERO_E_ALIAS;
-  }
-  GatherLaunch L;
-  L.shards = reinterpret_cast<const uint16_t* const*>(shard_ptrs);
-  L.world = N;
-  L.full = static_cast<uint16_t*>(full_bf16);
-  L.numel = unit_plan->numel;
-  L.shard = unit_plan->shard;
-  L.stream = static_cast<cudaStream_t>(stream);
-  L.withhold = g_withhold.load(std::memory_order_relaxed);
-  return launch_status(launch_unit_gather(L));
+  return launch_status(launch_unit_gather(pg.L));
 }
 
 int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t* cols,

@@ -76,5 +76,8 @@ cudaError_t launch_unit_gather(const GatherLaunch& L);
 // Status word of the TMA gather kernel's bounded waits; as above.
 int read_and_clear_gather_status(int* status);
 cudaError_t launch_unit_gather_rows(const GatherRowsLaunch& L);
+// The unit gather GL and the step L in one launch where both parts can run on
+// the TMA engine, else the two launches in that order; the same results.
+cudaError_t launch_unit_step(const GatherLaunch& GL, const StepLaunch& L);
 
 }  // namespace zeroadam

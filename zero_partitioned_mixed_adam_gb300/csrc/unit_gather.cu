@@ -12,6 +12,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "gather_ring.h"
 #include "internal.h"
 #include "tma_ops.h"
 
@@ -64,70 +65,20 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------------------------
-// The gathers on the TMA engine.  A copy is cut into chunks of up to 8192
-// elements (16 KB) whose pieces all start on 16-byte boundaries and are
-// multiples of 16 bytes long; the launchers check the layouts that guarantee
-// it.  One thread per CTA (one CTA per SM) moves its chunks (chunk
-// blockIdx.x + i * gridDim.x) through a 4-slot ring in shared memory: bulk
-// loads of a chunk's pieces into a slot, completing on the slot's mbarrier,
-// then one bulk store of the slot, committed as a bulk async-group.  Loads run
-// 3 chunks ahead; a slot is reloaded once the store that read it has finished
-// reading.  Elements that do not fill a 16-byte unit at the end of a run are
-// copied with plain loads and stores.  Measured against the load/store kernels
-// on GB300: the same bytes and about the same time under ncu; back to back,
-// the flat gather 1-3 % faster on units of 202M and 2^29 elements (0.93-0.98 of
-// the copy peak) and 1.5x on 2^24, 2.4x on 2^20 units with the L2 warm, the row
-// gather 3.5 % faster on a Llama-7B layer (0.94).
-//
-// Every wait is bounded by the global timer; a wait that gives up records a
-// nonzero status in g_gather_status (read with the step kernels' word by
-// zero_device_status), waits (bounded) for the loads already issued and for
-// its stores, and stops.
-
-constexpr int kChunk = 8192;  // elements per chunk
-constexpr int kSlots = 4;     // ring of 4 x 16 KB
-constexpr int64_t kSlotBytes = static_cast<int64_t>(kChunk) * 2;
-constexpr size_t kRingBytes = static_cast<size_t>(kSlots) * kSlotBytes;
+// The gathers on the TMA engine: one thread per CTA (one CTA per SM) moves
+// its chunks through a 4-slot ring in shared memory (ring_copy, the copy
+// shared with the fused unit step, gather_ring.h).  Elements that do not fill
+// a 16-byte unit at the end of a run are copied with plain loads and stores.
+// Measured against the load/store kernels on GB300: the same bytes and about
+// the same time under ncu; back to back, the flat gather 1-3 % faster on units
+// of 202M and 2^29 elements (0.93-0.98 of the copy peak) and 1.5x on 2^24,
+// 2.4x on 2^20 units with the L2 warm, the row gather 3.5 % faster on a
+// Llama-7B layer (0.94).  A wait that gives up records a nonzero status in
+// g_gather_status (read with the step kernels' word by zero_device_status).
 
 __device__ int g_gather_status;
 
-// One thread moves its CTA's `mine` chunks (chunk i of the CTA is chunk
-// blockIdx.x + i * gridDim.x of the copy) through the ring.  layout.load(i,
-// slot, bar) issues the bulk loads of the CTA's chunk i into `slot` and arms
-// `bar` with their byte count (zero bytes: the arrive alone completes the
-// phase); it is called for i = 0, 1, 2, ... in order.  layout.store(i, slot)
-// issues chunk i's bulk store, if it has any bytes.
-template <class Layout>
-__device__ void ring_copy(Layout& layout, int64_t mine, uint8_t* ring, uint64_t* bar,
-                          bool withhold) {
-  auto load = [&](int64_t i) {
-    if (!withhold) layout.load(i, ring + (i % kSlots) * kSlotBytes, &bar[i % kSlots]);
-  };
-  int64_t loaded = mine < kSlots - 1 ? mine : kSlots - 1;
-  for (int64_t i = 0; i < loaded; ++i) load(i);
-  for (int64_t i = 0; i < mine; ++i) {
-    const int s = static_cast<int>(i % kSlots);
-    if (!mbar_wait(&bar[s], static_cast<uint32_t>((i / kSlots) & 1))) {
-      atomicExch(&g_gather_status, 1);
-      for (int64_t j = i; j < loaded && !withhold; ++j)  // issued loads land first
-        mbar_wait(&bar[j % kSlots], static_cast<uint32_t>((j / kSlots) & 1));
-      break;
-    }
-    fence_async_shared();
-    layout.store(i, ring + s * kSlotBytes);
-    bulk_commit();
-    if (i + kSlots - 1 < mine) {
-      bulk_wait_read<1>();  // the store of chunk i - 1 has read slot (i - 1) % kSlots
-      load(i + kSlots - 1);
-      ++loaded;
-    }
-  }
-  bulk_wait_all();
-}
-
 // Flat gather: shard a multiple of 8 elements, every buffer 16-byte aligned.
-// The unit's first u8 = numel rounded down to 8 elements is chunked; a chunk
-// is one piece per shard it touches.
 template <int CAP>
 struct GatherTmaArgs {
   const uint16_t* src[CAP];
@@ -136,33 +87,6 @@ struct GatherTmaArgs {
   int64_t u8;     // numel rounded down to a multiple of 8: [0, u8) moves by TMA
   int64_t shard;  // a multiple of 8
   int32_t withhold;  // test hook: issue no loads, so every wait runs out
-};
-
-// The CTA's chunk i covers [e0, e1): e0 = (blockIdx.x + i * gridDim.x) * kChunk.
-template <int CAP>
-struct FlatLayout {
-  const GatherTmaArgs<CAP>& a;
-  __device__ void range(int64_t i, int64_t* e0, int64_t* e1) const {
-    *e0 = (blockIdx.x + i * static_cast<int64_t>(gridDim.x)) * kChunk;
-    *e1 = *e0 + kChunk < a.u8 ? *e0 + kChunk : a.u8;
-  }
-  __device__ void load(int64_t i, uint8_t* slot, uint64_t* bar) const {
-    int64_t e0, e1;
-    range(i, &e0, &e1);
-    mbar_expect_tx(bar, static_cast<uint32_t>((e1 - e0) * 2));
-    for (int64_t e = e0; e < e1;) {  // one piece per shard the chunk touches
-      const int64_t r = e / a.shard;
-      const int64_t pe = (r + 1) * a.shard < e1 ? (r + 1) * a.shard : e1;
-      bulk_load(slot + (e - e0) * 2, a.src[r] + (e - r * a.shard),
-                static_cast<uint32_t>((pe - e) * 2), bar);
-      e = pe;
-    }
-  }
-  __device__ void store(int64_t i, const uint8_t* slot) const {
-    int64_t e0, e1;
-    range(i, &e0, &e1);
-    bulk_store(a.full + e0, slot, static_cast<uint32_t>((e1 - e0) * 2));
-  }
 };
 
 template <int CAP>
@@ -181,8 +105,8 @@ __global__ void __launch_bounds__(32, 1)
   for (int s = 0; s < kSlots; ++s) mbar_init(&bar[s], 1);
   mbar_init_fence();
   const int64_t mine = (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
-  FlatLayout<CAP> layout{a};
-  ring_copy(layout, mine, ring, bar, a.withhold != 0);
+  FlatLayout<GatherTmaArgs<CAP>> layout{a};
+  ring_copy<kSlots>(layout, mine, ring, bar, a.withhold != 0, &g_gather_status);
 }
 
 template <int CAP>
@@ -218,7 +142,7 @@ bool launch_tma_cap(const GatherLaunch& L, cudaError_t* err) {
   a.u8 = u8;
   a.shard = L.shard;
   a.withhold = L.withhold;
-  const int64_t nchunks = (u8 + kChunk - 1) / kChunk;
+  const int64_t nchunks = flat_chunks(u8);
   const int grid = static_cast<int>(nchunks < sms ? nchunks : sms);
   zero3_unit_gather_tma_kernel<CAP><<<grid, 32, kRingBytes, L.stream>>>(a);
   *err = cudaGetLastError();
@@ -454,7 +378,7 @@ __global__ void __launch_bounds__(32, 1)
   const int64_t mine = (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
   RowsLayout layout{tb, src, g.full, pending, g.world, g.ntensors, 0, blockIdx.x, gridDim.x};
   layout.skip();
-  ring_copy(layout, mine, ring, bar, a.withhold != 0);
+  ring_copy<kSlots>(layout, mine, ring, bar, a.withhold != 0, &g_gather_status);
 }
 
 template <int CAP>
