@@ -211,29 +211,29 @@ class Replica:
 
     def unit_step_kernel_name(self):
         """zero3_unit_step runs the gather and the step as one launch when the shard
-        is a multiple of 8 elements and every buffer is 16-byte aligned at its first
-        element; otherwise the gather kernel, then the step kernel."""
+        is a multiple of 8 elements, every buffer is 16-byte aligned at its first
+        element and the unit moves at most 512 MiB (256 MiB at N >= 40); otherwise
+        the gather kernel, then the step kernel."""
         aligned = all(x.data_ptr() % 16 == 0
                       for x in self.shards + [self.full] + self.g + [self.w, self.m, self.v,
                                                                      self.p])
-        if self.wl.numel >= 8 and self.n >= 8 and self.plan.shard % 8 == 0 and aligned:
+        limit = (512 if self.wl.world < 40 else 256) << 20
+        small = 4 * self.wl.numel + _bytes_per_step(self.wl, self.plan) <= limit
+        if self.wl.numel >= 8 and self.n >= 8 and self.plan.shard % 8 == 0 and aligned and small:
             return "zero3_unit_step_kernel"
         return f"{self.gather_kernel_name()}+{self.step_kernel_name()}"
 
     def step_kernel_name(self):
-        """The library runs a TMA-staged kernel for N = 16 (gradients and state
-        staged) and every other N >= 5 (gradients staged in rank groups) when
-        every buffer is 16-byte aligned at the range's first element (whole
-        cudaMalloc buffers); the register-staged kernel otherwise."""
+        """The library runs the TMA-staged kernel (gradients staged in rank groups)
+        for N >= 5 when every buffer is 16-byte aligned at the range's first
+        element (whole cudaMalloc buffers); the register-staged kernel otherwise."""
         def aligned(t, first, esize):
             return (t.data_ptr() + first * esize) % 16 == 0
         tma = (self.wl.world >= 5 and self.n >= 8
                and all(aligned(g, self.g_first, 2) for g in self.g)
                and all(aligned(x, 0, 4) for x in (self.w, self.m, self.v))
                and aligned(self.p, self.p_first, 2))
-        if not tma:
-            return "zero_adam_step_kernel"
-        return "zero_adam_step_tma_kernel" if self.wl.world == 16 else "zero_adam_step_tma_grad_kernel"
+        return "zero_adam_step_tma_grad_kernel" if tma else "zero_adam_step_kernel"
 
     def fill_grads(self, t):
         import torch

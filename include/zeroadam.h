@@ -264,10 +264,13 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
  * shard_ptrs[rank]) call the two functions in sequence instead.
  *
  * When the shard is a multiple of 8 elements, every buffer of both parts is
- * 16-byte aligned at its first element, the gradients are bf16 and the sum is
- * fp32, the single launch runs (bulk copies on the TMA engine, bounded waits
- * reported by zero_device_status); otherwise the two kernels are launched in
- * order on the stream.  Errors: those of zero3_unit_gather and
+ * 16-byte aligned at its first element, the gradients are bf16, the sum is
+ * fp32 and the unit moves at most 512 MiB (gather 4 bytes per unit element +
+ * step (2*world + 26) bytes per stepped element; 256 MiB at world >= 40), the
+ * single launch runs (bulk copies on the TMA engine, bounded waits reported by
+ * zero_device_status); otherwise the two kernels are launched in order on the
+ * stream (larger units stream as fast that way, with the launch cost
+ * amortised).  Errors: those of zero3_unit_gather and
  * zero_adam_step (ZERO_GRAD_WINDOW is not accepted: ZERO_E_LAYOUT).
  */
 int zero3_unit_step(const zero_plan_t* unit_plan, int32_t rank, const void* const* shard_ptrs,

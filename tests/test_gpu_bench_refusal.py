@@ -23,7 +23,7 @@ def test_timed_region_with_a_given_up_wait_is_refused():
     dev = torch.device("cuda", 0)
     wl = C.StepWorkload("probe_n16", numel=1_000_003, world=16)
     rep = bench.Replica(wl, dev)
-    assert rep.step_kernel_name() == "zero_adam_step_tma_kernel"
+    assert rep.step_kernel_name() == "zero_adam_step_tma_grad_kernel"
     stream = torch.cuda.current_stream(dev)
     rep.fill_grads(1)
     assert bench.device_verdict(za) == "ok"

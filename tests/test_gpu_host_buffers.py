@@ -1,8 +1,8 @@
 """The end-to-end path with host buffers: gradients in pinned host memory and the
 bf16 parameters written to pinned host memory, read and written by the kernels
 directly (NVLink-C2C on GB300).  The result must equal the all-device step bit
-for bit, on the register-staged kernel (N = 4) and the TMA-staged ones (N = 8 and
-N = 64, gradients staged in rank groups; N = 16, gradients and state staged)."""
+for bit, on the register-staged kernel (N = 4) and the TMA-staged one (N = 8, 16
+and 64: gradients staged in rank groups of 8 and of 32)."""
 import pytest
 import torch
 

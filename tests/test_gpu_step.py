@@ -453,14 +453,15 @@ def test_zero_gradients_and_signed_zeros(eps):
         assert np.isnan(gu.to_host_f32(pr.w)[:numel][zero_rows]).all()
 
 
-# TMA-staged kernel tiles: 2048 elements at N = 16 (gradients and state staged); the
-# gradient-staged kernel's 3072 at 5 <= N < 40 (rank groups of 8) and 1024 at N >= 40
-# (rank groups of 32), including N whose last rank group is partial (5, 12, 33, 100)
-STAGED = ([(16, n) for n in (8, 13, 2048 * 16 + 8, 2048 * 152 * 2 + 5, 4_000_037)]
-          + [(8, n) for n in (8, 13, 3072 * 8 + 8, 3072 * 152 * 3 + 5, 3072 * 152 + 3072 - 8,
+# The TMA-staged kernel's tiles: 2816 elements at 5 <= N < 40 (rank groups of 8) and
+# 1024 at N >= 40 (rank groups of 32), including N whose last rank group is partial
+# (5, 12, 33, 100)
+T8 = 22 * 32 * 4
+STAGED = ([(16, n) for n in (8, 13, T8 * 16 + 8, T8 * 152 * 2 + 5, 4_000_037)]
+          + [(8, n) for n in (8, 13, T8 * 8 + 8, T8 * 152 * 3 + 5, T8 * 152 + T8 - 8,
                               4_000_037)]
-          + [(5, n) for n in (8, 13, 3072 * 152 * 2 + 5, 1_000_037)]
-          + [(12, n) for n in (3072 * 3 + 8, 500_003)]
+          + [(5, n) for n in (8, 13, T8 * 152 * 2 + 5, 1_000_037)]
+          + [(12, n) for n in (T8 * 3 + 8, 500_003)]
           + [(33, n) for n in (8, 100_003)]
           + [(64, n) for n in (8, 13, 1024 * 64 + 8, 1024 * 152 * 2 + 5, 1024 * 152 + 1024 - 8,
                                1_000_037)]
@@ -469,8 +470,8 @@ STAGED = ([(16, n) for n in (8, 13, 2048 * 16 + 8, 2048 * 152 * 2 + 5, 4_000_037
 
 @pytest.mark.parametrize("world,numel", STAGED)
 def test_staged_path_sizes(world, numel):
-    """Aligned buffers take the TMA-staged kernels (gradients and state staged at
-    N = 16, gradients staged in rank groups at every other N >= 5): partial last tiles,
+    """Aligned buffers take the TMA-staged kernel (gradients staged in rank groups at
+    N >= 5): partial last tiles,
     fewer tiles than SMs, more tiles than SMs with a ragged last round, a partial last
     rank group, a scalar tail; two steps against the oracle, and the device status
     word stays clear."""

@@ -184,9 +184,10 @@ def test_unit_step_offset_buffers(off, N):
 
 @pytest.mark.parametrize("U", C.UNIT_SIZES)
 @pytest.mark.parametrize("N", C.UNIT_WORLDS)
-def test_unit_sweep_single_launch(U, N):
-    """The sweep's units at full size through the single launch, rank 0, two steps:
-    the whole unit against the oracle's gather, the step on the sampled windows."""
+def test_unit_sweep_unit_step(U, N):
+    """The sweep's units at full size through zero3_unit_step, rank 0, two steps (the
+    2^20 and 2^24 units as the single launch, the larger ones as two launches): the
+    whole unit against the oracle's gather, the step on the sampled windows."""
     plan = za.zero_plan(U, N)
     S = plan.shard
     shards = [torch.empty(S, dtype=torch.int16, device="cuda") for _ in range(N)]

@@ -12,10 +12,9 @@
 // parameter) bytes and does ~20 fp32 operations: it is bound by HBM
 // bandwidth, so it is written as a streaming kernel (16-byte vector
 // loads/stores, a persistent grid-stride loop of 512-thread blocks sized to
-// the SM count) and uses no tensor cores.  With aligned buffers, TMA-staged
-// variants (bulk copies into a shared-memory ring, one CTA per SM) replace it:
-// gradients and state staged at N = 16, gradients staged in rank groups at
-// every other N >= 5.
+// the SM count) and uses no tensor cores.  At N >= 5 with aligned buffers a
+// TMA-staged variant replaces it: the gradients are bulk-copied in rank groups
+// into a shared-memory ring, one CTA per SM.
 //
 // Bit-exactness: every operation is an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nvcc cannot contract any
@@ -96,11 +95,6 @@ __device__ __forceinline__ void accumulate_bf16x8(float acc[8], const uint4 r) {
   acc[7] = __fadd_rn(acc[7], bf16_hi(r.w));
 }
 
-__device__ __forceinline__ void unpack8(const float4 a, const float4 b, float x[8]) {
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
 // One step of the running sum over ranks.
 template <bool ABF16>
 __device__ __forceinline__ float acc_add(float acc, float x) {
@@ -128,6 +122,32 @@ __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, f
   const float denom = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
   const float num = __fmul_rn(s.lr, m_hat);
   w = __fsub_rn(w, (num == 0.0f && denom > 0.0f) ? num : __fdiv_rn(num, denom));
+}
+
+// The same update with the zero-numerator shortcut taken without a branch:
+// every lane runs the three divisions on normal operands (1.0 stands in for a
+// zero numerator, and 1/1 for the last division's shortcut case), then
+// selects the shortcut's result.  The values are those of adam_element bit
+// for bit.  The staged kernels use this form: with some exact-zero gradients
+// (the GPT-2 workload's 10 % mask) the branching form diverges within warps,
+// and the staged kernels' best consumer count then moved with the fraction of
+// zeros (measured on GB300 at N = 8: 24 warps 1.00-1.05 of the copy peak
+// depending on the data, this form 1.03-1.05 at 22 warps).
+__device__ __forceinline__ void adam_element_uniform(float gsum, const AdamScalars& s, float& w,
+                                                     float& m, float& v) {
+  const float g = s.pow2_world ? __fmul_rn(gsum, s.inv_world) : __fdiv_rn(gsum, s.world);
+  m = __fadd_rn(__fmul_rn(m, s.b1), __fmul_rn(s.omb1, g));
+  v = __fadd_rn(__fmul_rn(v, s.b2), __fmul_rn(__fmul_rn(s.omb2, g), g));
+  const bool mz = m == 0.0f, vz = v == 0.0f;
+  const float mq = __fdiv_rn(mz ? 1.0f : m, s.bc1);
+  const float vq = __fdiv_rn(vz ? 1.0f : v, s.bc2);
+  const float m_hat = mz ? m : mq;
+  const float v_hat = vz ? v : vq;
+  const float denom = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
+  const float num = __fmul_rn(s.lr, m_hat);
+  const bool z = num == 0.0f && denom > 0.0f;
+  const float q = __fdiv_rn(z ? 1.0f : num, z ? 1.0f : denom);
+  w = __fsub_rn(w, z ? num : q);
 }
 
 // 8 gradients of one rank as fp32, loaded as 16-byte vectors.
@@ -278,212 +298,39 @@ __global__ void __launch_bounds__(kThreads)
     step_element<NT, CAP, GF32, ABF16>(a, world, e);
 }
 
-// ---------------------------------------------------------------------------
-// TMA-staged variant for N = 16, bf16 gradients, fp32 sum (measured faster
-// than the register-staged kernel there; at other N the state-staged ring
-// leaves room for too few consumer warps, and zero_adam_step_tma_grad_kernel
-// below is used instead).
-// One CTA per SM.  Warp 0 lane 0 is the producer: for each 2048-element tile
-// it issues one bulk copy (cp.async.bulk, the TMA engine) per rank's gradient
-// tile and per state array into a two-stage shared-memory ring, and the
-// stage's mbarrier completes when all bytes have landed.  Warps 1..8 consume:
-// each thread sums its 8 elements over the ranks and runs adam_element from
-// shared memory, then stores to global.  Every wait is bounded by about one
-// second of the GPU's global timer; a wait that gives up records a nonzero
-// status in g_step_status (read by zero_device_status), the producer waits
-// (bounded) for the copies it issued, and every thread returns.
-
-constexpr int kTmaTile = 2048;       // elements per tile
-constexpr int kTmaConsumers = 256;   // 8 warps, 8 elements per thread
-constexpr int kTmaStages = 2;
-
+// Status word of the staged kernels' bounded waits (read and cleared by
+// zero_device_status): nonzero once a wait has given up.
 __device__ int g_step_status;
 
-template <int NT>
-struct TmaArgs {
-  const uint16_t* g[NT];
-  float* master;
-  float* m;
-  float* v;
-  uint16_t* param;
-  int64_t n;      // elements in the range
-  int64_t nbody;  // multiple of 8: [0, nbody) through the ring, [nbody, n) scalar
-  int32_t withhold;  // test hook: the producer issues no copies, so every wait runs out
-  AdamScalars s;
-};
-
-template <int NT>
-__global__ void __launch_bounds__(kTmaConsumers + 32, 1)
-    zero_adam_step_tma_kernel(const __grid_constant__ TmaArgs<NT> a) {
-  // stage: NT bf16 gradient tiles, then the master, m and v fp32 tiles
-  constexpr int64_t kGradBytes = kTmaTile * 2;
-  constexpr int64_t kStage = NT * kGradBytes + 3 * kTmaTile * 4;
-  extern __shared__ __align__(1024) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[kTmaStages], empty[kTmaStages];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t ntiles = (a.nbody + kTmaTile - 1) / kTmaTile;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kTmaStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kTmaConsumers / 32);
-    }
-    mbar_init_fence();
-  }
-  __syncthreads();
-
-  if (warp == 0) {
-    if (lane != 0) return;
-    int64_t k = 0;
-    bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
-      const int s = static_cast<int>(k % kTmaStages);
-      if (k >= kTmaStages &&
-          !mbar_wait(&empty[s], static_cast<uint32_t>((k / kTmaStages - 1) & 1))) {
-        ok = false;
-        break;
-      }
-      if (a.withhold) continue;
-      const int64_t e0 = tile * kTmaTile;
-      int64_t cnt = a.nbody - e0;
-      if (cnt > kTmaTile) cnt = kTmaTile;
-      const uint32_t gbytes = static_cast<uint32_t>(cnt * 2);
-      uint8_t* st = ring + s * kStage;
-      mbar_expect_tx(&full[s], gbytes * NT + 3 * 2 * gbytes);
-      for (int r = 0; r < NT; ++r) bulk_load(st + r * kGradBytes, a.g[r] + e0, gbytes, &full[s]);
-      uint8_t* sf = st + NT * kGradBytes;
-      bulk_load(sf, a.master + e0, 2 * gbytes, &full[s]);
-      bulk_load(sf + kTmaTile * 4, a.m + e0, 2 * gbytes, &full[s]);
-      bulk_load(sf + 2 * kTmaTile * 4, a.v + e0, 2 * gbytes, &full[s]);
-    }
-    if (!ok) {
-      atomicExch(&g_step_status, 1);
-      const int64_t first = k > kTmaStages ? k - kTmaStages : 0;
-      for (int64_t j = first; j < k && !a.withhold; ++j)
-        mbar_wait(&full[j % kTmaStages], static_cast<uint32_t>((j / kTmaStages) & 1));
-    }
-    return;
-  }
-
-  const int t = threadIdx.x - 32;
-  int64_t k = 0;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
-    const int s = static_cast<int>(k % kTmaStages);
-    if (!mbar_wait(&full[s], static_cast<uint32_t>((k / kTmaStages) & 1))) {
-      atomicExch(&g_step_status, 2);
-      return;
-    }
-    const int64_t e0 = tile * kTmaTile + 8 * t;
-    const bool in = e0 < a.nbody;  // e0 and nbody are multiples of 8
-    const uint8_t* st = ring + s * kStage;
-    float acc[8], w[8], mm[8], vv[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = -0.0f;
-    if (in) {
-#pragma unroll
-      for (int r = 0; r < NT; ++r)
-        accumulate_bf16x8(acc, *reinterpret_cast<const uint4*>(st + r * kGradBytes + 16 * t));
-      const float4* sf = reinterpret_cast<const float4*>(st + NT * kGradBytes);
-      unpack8(sf[2 * t], sf[2 * t + 1], w);
-      unpack8(sf[kTmaTile / 4 + 2 * t], sf[kTmaTile / 4 + 2 * t + 1], mm);
-      unpack8(sf[kTmaTile / 2 + 2 * t], sf[kTmaTile / 2 + 2 * t + 1], vv);
-    }
-    // every lane has read its slice of stage s: the warp hands the stage back
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (in) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) adam_element(acc[j], a.s, w[j], mm[j], vv[j]);
-      store_f32x8(a.master + e0, true, w);
-      store_f32x8(a.m + e0, true, mm);
-      store_f32x8(a.v + e0, true, vv);
-      store_bf16x8_rn(a.param + e0, true, w);
-    }
-  }
-  // the last few (< 8) elements of the range, one per thread of block 0
-  if (blockIdx.x == 0 && a.nbody + t < a.n) {
-    const int64_t e = a.nbody + t;
-    float acc = -0.0f;
-#pragma unroll
-    for (int r = 0; r < NT; ++r) acc = __fadd_rn(acc, bf16_to_f32(ld_grad(a.g[r] + e)));
-    float w = ld_state(a.master + e), mm = ld_state(a.m + e), vv = ld_state(a.v + e);
-    adam_element(acc, a.s, w, mm, vv);
-    a.master[e] = w;
-    a.m[e] = mm;
-    a.v[e] = vv;
-    a.param[e] = f32_to_bf16_rn(w);
-  }
-}
-
-constexpr size_t tma_smem_bytes(int nt) {
-  return static_cast<size_t>(kTmaStages) * (nt * kTmaTile * 2 + 3 * kTmaTile * 4);
-}
-
-// Launch the TMA kernel when every buffer is 16-byte aligned at the range's
-// first element (head == 0 with all streams vectorised).  Returns false when
-// the variant does not apply.
-template <int NT>
-bool launch_tma(const StepLaunch& L, const StepArgs<NT>& a, cudaError_t* err) {
-  if (!(a.head == 0 && a.gvec && a.svec && a.pvec) || a.nvec < 1) return false;
-  static std::mutex mu;
-  static bool configured[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!configured[dev]) {
-      if (cudaFuncSetAttribute(zero_adam_step_tma_kernel<NT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tma_smem_bytes(NT))) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
-      }
-      configured[dev] = true;
-    }
-  }
-  int sms = 0;
-  if (device_sm_count(&sms) != 0) return false;
-  TmaArgs<NT> t;
-  for (int k = 0; k < NT; ++k) t.g[k] = static_cast<const uint16_t*>(L.grads[k]);
-  t.master = L.master;
-  t.m = L.m;
-  t.v = L.v;
-  t.param = L.param;
-  t.n = L.n;
-  t.nbody = 8 * a.nvec;
-  t.withhold = L.withhold;
-  t.s = L.s;
-  const int64_t ntiles = (t.nbody + kTmaTile - 1) / kTmaTile;
-  const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
-  zero_adam_step_tma_kernel<NT>
-      <<<grid, kTmaConsumers + 32, tma_smem_bytes(NT), L.stream>>>(t);
-  *err = cudaGetLastError();
-  return true;
-}
-
 // ---------------------------------------------------------------------------
-// TMA-staged gradients, register-staged state: the variant for every other
-// N >= 5 (bf16 gradients, fp32 sum, buffers 16-byte aligned).  One CTA per SM.
-// A tile of TILE = CW*32*EPT elements is reduced over the ranks in groups of
-// G: ring stage k holds G ranks' gradient tiles (G bulk copies of TILE*2
-// bytes, cp.async.bulk on the TMA engine), so a tile passes through
-// ceil(N/G) stages and the ring depth in bytes does not grow with N.  Warp 0
-// is the producer: lane 0 arms the stage's mbarrier with its byte count, then
-// lane r issues rank r's copy, so N copies per tile go out in parallel
-// instead of from one thread.  The CW consumer warps' threads each own EPT
-// consecutive elements of the tile: they load their master, m and v into
-// registers (16- or 8-byte loads) before they wait for the first group, so
-// those loads overlap the gradient copies; they add the groups in rank order
-// from shared memory, hand each stage back, and after the last group run
-// adam_element and store.  Waits are bounded as in the kernel above, with the
-// same status word.
+// TMA-staged gradients, register-staged state: the variant for N >= 5 (bf16
+// gradients, fp32 sum, buffers 16-byte aligned).  One CTA per SM.  A tile of
+// TILE = CW*32*EPT elements is reduced over the ranks in groups of G: ring
+// stage k holds G ranks' gradient tiles (G bulk copies of TILE*2 bytes,
+// cp.async.bulk on the TMA engine), so a tile passes through ceil(N/G) stages
+// and the ring depth in bytes does not grow with N.  Warp 0 is the producer:
+// lane 0 arms the stage's mbarrier with its byte count, then lane r issues
+// rank r's copy, so N copies per tile go out in parallel instead of from one
+// thread.  The CW consumer warps' threads each own EPT consecutive elements of
+// the tile: they load their master, m and v into registers (16- or 8-byte
+// loads) before they wait for the first group, so those loads overlap the
+// gradient copies; they add the groups in rank order from shared memory, hand
+// each stage back, and after the last group run adam_element_uniform and
+// store.  Every wait is bounded by about one second of the GPU's global timer;
+// a wait that gives up records a nonzero status in g_step_status (read by
+// zero_device_status), the producer waits (bounded) for the copies it issued,
+// and every thread returns.
 //
 // Two shapes, chosen by N (measured on GB300 against the register-staged
-// kernel, bit-exact in every case): G = 8, EPT = 4, 24 consumer warps, 3
-// stages of 48 KB for 5 <= N < 40 (N = 5: 0.68 -> 0.91 of the copy peak,
-// N = 12: 0.72 -> 1.02, N = 32: 0.93 -> 0.96 on a 6.3M-element shard; equal to
-// the earlier N = 8-only kernel, which had this shape with one issuing
-// thread); G = 32, EPT = 2, 16 consumer warps, 3 stages of 64 KB for N >= 40
-// (N = 64: 0.92 -> 0.975 on a 3.16M-element shard, 0.99 -> 1.00 on 8.4M).
+// kernel, bit-exact in every case): G = 8, EPT = 4, 22 consumer warps, 3
+// stages of 44 KB for 5 <= N < 40 (N = 5: 0.68 -> 0.93 of the copy peak,
+// N = 12: 0.72 -> 1.02, N = 32: 0.93 -> 1.03 on a 16.8M-element shard; at N = 8
+// 1.03-1.05 with and without exact-zero gradients; at N = 16 1.058 on the 1.3B
+// workload, level with an earlier kernel that also staged master/m/v through
+// the ring behind 8 consumer warps, which fell to 0.86 when 10 % of the
+// gradients were exact zeros while this one held 1.06); G = 32, EPT = 2, 16
+// consumer warps, 3 stages of 64 KB for N >= 40 (N = 64: 0.92 -> 0.975 on a
+// 3.16M-element shard, 0.99 -> 1.00 on 8.4M).
 
 template <int CAP>
 struct GradStagedArgs {
@@ -660,7 +507,7 @@ __device__ bool grad_stage_consumer(const GradStagedArgs<CAP>& a, const uint8_t*
     }
     if (in) {
 #pragma unroll
-      for (int j = 0; j < EPT; ++j) adam_element(acc[j], a.s, w[j], mm[j], vv[j]);
+      for (int j = 0; j < EPT; ++j) adam_element_uniform(acc[j], a.s, w[j], mm[j], vv[j]);
       store_state_vec<EPT>(a.master + e0, w);
       store_state_vec<EPT>(a.m + e0, mm);
       store_state_vec<EPT>(a.v + e0, vv);
@@ -754,9 +601,9 @@ bool launch_tma_grad_shape(const StepLaunch& L, int64_t nbody, cudaError_t* err)
 // not apply.
 bool launch_tma_grad(const StepLaunch& L, int32_t head, int64_t nvec, bool all_vec,
                      cudaError_t* err) {
-  if (!(head == 0 && all_vec) || nvec < 1 || L.world < 5 || L.world == 16) return false;
+  if (!(head == 0 && all_vec) || nvec < 1 || L.world < 5) return false;
   const int64_t nbody = 8 * nvec;
-  if (L.world < 40) return launch_tma_grad_shape<8, 4, 24, 3, 64>(L, nbody, err);
+  if (L.world < 40) return launch_tma_grad_shape<8, 4, 22, 3, 64>(L, nbody, err);
   if (L.world <= 64) return launch_tma_grad_shape<32, 2, 16, 3, 64>(L, nbody, err);
   return launch_tma_grad_shape<32, 2, 16, 3, kTableRuntime>(L, nbody, err);
 }
@@ -994,10 +841,6 @@ cudaError_t launch_world(const StepLaunch& L) {
   a.svec = (rs >= 0 && (rs + best_h) % 4 == 0);
   a.pvec = ((rp + best_h) % 8 == 0);
 
-  if constexpr (NT == 16 && CAP == 16 && !GF32 && !ABF16) {
-    cudaError_t err = cudaSuccess;
-    if (launch_tma<16>(L, a, &err)) return err;
-  }
   if constexpr (!GF32 && !ABF16) {
     cudaError_t err = cudaSuccess;
     if (launch_tma_grad(L, a.head, a.nvec, a.gvec && a.svec && a.pvec, &err)) return err;
@@ -1029,11 +872,26 @@ cudaError_t launch_variant(const StepLaunch& L) {
   }
 }
 
+// Largest unit (gather bytes + step bytes) that takes the single launch.
+// Measured on GB300 against the gather and the step as two launches, units
+// of 2^22..2^27 elements with the L2 flushed: at N = 2 and 8 the single launch
+// takes 0.71-0.87 of the time up to 320 MB and 0.95-0.98 at 620 MB, and
+// 1.01-1.03 at 1.2 GB; at N = 64 (two gather slots beside the larger step
+// ring) 0.62-0.96 up to 215 MB and 1.14 at 430 MB.  Past these sizes each
+// kernel alone streams at its own best and the launch cost is amortised,
+// while inside the single launch the gather's ring falls behind the step's
+// consumers and finishes alone.
+constexpr int64_t kFusedMaxBytes = int64_t{512} << 20;
+constexpr int64_t kFusedMaxBytesLargeN = int64_t{256} << 20;
+
 // The fused unit step when both parts can run on the TMA engine: the gather's
 // shard a multiple of 8 elements, and every buffer of both parts 16-byte
-// aligned at its first element; bf16 gradients, fp32 sum.
+// aligned at its first element; bf16 gradients, fp32 sum; a unit below the
+// size limit above.
 bool launch_unit_step_fused(const GatherLaunch& GL, const StepLaunch& L, cudaError_t* err) {
   if (L.grad_f32 || L.acc_bf16 || L.n < 8 || GL.numel < 8 || GL.shard % 8 != 0) return false;
+  const int64_t bytes = 4 * GL.numel + (2 * static_cast<int64_t>(L.world) + 26) * L.n;
+  if (bytes > (L.world < 40 ? kFusedMaxBytes : kFusedMaxBytesLargeN)) return false;
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   bool ok = a16(GL.full) && a16(L.master) && a16(L.m) && a16(L.v) && a16(L.param);
   for (int k = 0; k < GL.world && ok; ++k) ok = a16(GL.shards[k]);
@@ -1041,7 +899,7 @@ bool launch_unit_step_fused(const GatherLaunch& GL, const StepLaunch& L, cudaErr
   if (!ok) return false;
   const int64_t nbody = L.n & ~static_cast<int64_t>(7);
   if (L.world <= 4) return launch_unit_step_shape<1, 8, 24, 1, 4, 64, true>(GL, L, nbody, err);
-  if (L.world < 40) return launch_unit_step_shape<8, 4, 24, 3, 4, 64, false>(GL, L, nbody, err);
+  if (L.world < 40) return launch_unit_step_shape<8, 4, 22, 3, 4, 64, false>(GL, L, nbody, err);
   if (L.world <= 64) return launch_unit_step_shape<32, 2, 16, 3, 2, 64, false>(GL, L, nbody, err);
   return launch_unit_step_shape<32, 2, 16, 3, 2, kTableRuntime, false>(GL, L, nbody, err);
 }
