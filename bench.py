@@ -55,6 +55,10 @@ def _workload(name):
         # unit:<U>:<N>
         _, u, n = name.split(":")
         return C.unit_workload(int(u), int(n))
+    if name.startswith("shard:"):
+        # shard:<U>:<N>: the unit's rank-0 step alone, without the gather before it
+        _, u, n = name.split(":")
+        return C.unit_shard_step_workload(int(u), int(n))
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -130,26 +134,35 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def code_hash(path):
-    """SHA-256 of a C++/CUDA source with its // comments, trailing blanks and empty
+def code_hash(*paths):
+    """SHA-256 of C++/CUDA sources with their // comments, trailing blanks and empty
     lines removed: it changes when the code does, not when a comment does."""
     lines = []
-    with open(path, encoding="utf-8") as f:
-        for line in f:
-            code = line.split("//", 1)[0].rstrip()
-            if code:
-                lines.append(code)
+    for path in paths:
+        with open(path, encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    lines.append(code)
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
+def kernel_source_hash(kernel_src):
+    """code_hash of a kernel file together with every header of the library's sources
+    (the kernels' shared device code lives in them)."""
+    csrc = os.path.dirname(kernel_src)
+    headers = sorted(os.path.join(csrc, h) for h in os.listdir(csrc) if h.endswith(".h"))
+    return code_hash(kernel_src, *headers)
 
 
 def _traffic_record(kernel_src):
     """DRAM traffic per element from the committed ncu summary, if it was taken on
-    the current code of the kernel's source file (else None)."""
+    the current code of the kernel's source file and headers (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        return rec.get(code_hash(kernel_src))
+        return rec.get(kernel_source_hash(kernel_src))
     except Exception:
         return None
 
@@ -538,7 +551,8 @@ def run_ours(args, wl):
     require_ok(device_verdict(rep.za, dist, dev), "prewarm and warm-up steps")
 
     nk = len(rep.kernels)
-    flush = L2Flush(dev) if L2Flush.needed(rep.step_bytes(), dev) else None
+    need = L2Flush.needed(rep.step_bytes(), dev) if args.l2 == "auto" else args.l2 == "flush"
+    flush = L2Flush(dev) if need else None
     sampler = ClockSampler(local)
     sampler.start()
     t, ev, wall = timed_region(rep, stream, args.steps, t, flush, dist)
@@ -1033,7 +1047,7 @@ def main(argv=None):
                     help="reference: the CPU oracle on the host cores")
     ap.add_argument("--workload", default="1p3b",
                     help="1p3b | gpt2 | 7b_rank3 | 7b_rank3_prewarm | tiny | unit:U:N | "
-                         "zero2_buckets | zero3_prefetch")
+                         "shard:U:N | zero2_buckets | zero3_prefetch")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run")
     ap.add_argument("--e2e-steps", type=int, default=5, help="steps of the host-buffer run")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
@@ -1043,6 +1057,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=8, help="zero3_prefetch: units per pass")
     ap.add_argument("--prefetch-world", type=int, default=8, help="zero3_prefetch: ranks")
     ap.add_argument("--tokens", type=int, default=4096, help="zero3_prefetch: GEMM rows")
+    ap.add_argument("--l2", choices=("auto", "flush", "none"), default="auto",
+                    help="flush the L2 before every timed step: auto = when a step moves less "
+                         "than four L2 sizes")
     ap.add_argument("--unit-mode", choices=("fused", "separate"), default="fused",
                     help="unit workloads: one zero3_unit_step call, or the gather and the "
                          "step as two calls")

@@ -109,6 +109,13 @@ def unit_workload(unit_numel: int, world: int) -> StepWorkload:
                         grad_layout="shard", param_layout="shard", steps=1)
 
 
+def unit_shard_step_workload(unit_numel: int, world: int) -> StepWorkload:
+    """The same unit's rank-0 step alone (no gather before it): the step measured on
+    its own, with the same inputs as unit_workload's step."""
+    return StepWorkload(f"shard{unit_numel}_n{world}", numel=unit_numel, world=world, rank=0,
+                        grad_layout="shard", param_layout="shard", steps=1)
+
+
 def unit_shard_spec(unit_numel: int, world: int, r: int) -> Spec:
     """Rank r's bf16 parameter shard of a ZeRO-3 unit (input of the gather)."""
     return Spec(seed=unit_numel % 1000003 + world, stream=STREAM_PARAM_SHARD, rank=r, sigma=0.02)

@@ -9,6 +9,20 @@ import bench
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+def test_kernel_source_hash_covers_the_headers(tmp_path):
+    """A change in a shared header (where part of a kernel's device code lives) voids
+    the kernel's records; a comment change does not."""
+    cu = tmp_path / "k.cu"
+    cu.write_text("int k() { return f(); }\n")
+    h = tmp_path / "ops.h"
+    h.write_text("inline int f() { return 1; }\n")
+    first = bench.kernel_source_hash(str(cu))
+    h.write_text("inline int f() { return 1; }  // note\n")
+    assert bench.kernel_source_hash(str(cu)) == first
+    h.write_text("inline int f() { return 2; }\n")
+    assert bench.kernel_source_hash(str(cu)) != first
+
+
 def test_code_hash_ignores_comments_not_code(tmp_path):
     a = tmp_path / "a.cu"
     a.write_text("int f(int x) {\n  return x + 1;  // one more\n}\n")
@@ -30,10 +44,18 @@ def test_records_are_consistent():
         assert len(key) == 64
         for name, r in kernels.items():
             kernel, world = name.split("/N")
-            assert kernel.startswith(("zero_adam_step", "zero3_unit_gather")) and int(world) >= 1
+            assert kernel.startswith(("zero_adam_step", "zero3_unit_gather", "zero3_unit_step"))
+            assert int(world) >= 1
             per = (r["dram_read_bytes"] + r["dram_write_bytes"]) / r["elements"]
             assert abs(per - r["dram_bytes_per_element"]) < 1e-4
-            # writes still in L2 at the kernel's end make it a little below the algorithmic bytes
-            assert 0.85 * r["algorithmic_bytes_per_element"] < per <= 1.02 * r["algorithmic_bytes_per_element"]
+            # every input byte is read once: the reads match the algorithmic reads
+            reads = r["dram_read_bytes"] / r["elements"]
+            alg_r = r["algorithmic_read_bytes_per_element"]
+            assert 0.98 * alg_r <= reads <= 1.02 * alg_r, name
+            # writes still in L2 at the kernel's end make the total a little below the
+            # algorithmic bytes (far below for a launch whose working set is near L2's size)
+            alg = r["algorithmic_bytes_per_element"]
+            lower = 0.5 if r.get("writes_in_l2") else 0.85
+            assert lower * alg < per <= 1.02 * alg, name
             n += 1
-    assert n >= 5
+    assert n >= 4
