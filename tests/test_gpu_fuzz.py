@@ -157,3 +157,34 @@ def test_row_gather_sweep(shapes, world, seed):
     torch.cuda.synchronize()
     assert (gu.to_host_u16(full) == oracle.unit_gather_rows(shapes, world, host)).all()
     assert za.device_status() == za.ZERO_OK
+
+
+def _unit_step_cases(n=32, seed=17):
+    """Units whose shard is a multiple of 8 half the time (the one-launch path when every
+    buffer is aligned), any rank, both gradient and parameter layouts, and offsets that keep
+    or break the 16-byte alignment."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        world = int(rng.choice(WORLDS))
+        if i % 2:
+            U = int(rng.integers(1, 40_000)) * 8 * world - int(rng.integers(0, 8))
+        else:
+            U = int(rng.integers(world, 300_000))
+        U = max(U, 1)
+        rank = int(rng.integers(0, world))
+        gl = FULL if rng.random() < 0.3 else SHARD
+        pl = za.ZERO_PARAM_FULL if rng.random() < 0.3 else za.ZERO_PARAM_SHARD
+        off = int(rng.choice([0, 0, 0, 8, 1, 3]))
+        cases.append((U, world, rank, gl, pl, off, i))
+    return cases
+
+
+@pytest.mark.parametrize("U,world,rank,gl,pl,off,seed", _unit_step_cases())
+def test_unit_step_sweep(U, world, rank, gl, pl, off, seed):
+    from test_gpu_unit_step import UnitProblem
+    pr = UnitProblem(U, world, rank=rank, grad_layout=gl, param_layout=pl, off=off, seed=seed)
+    for t in (1, 2):
+        pr.step(t)
+        pr.check(f"unit step fuzz {seed} t={t}")
+    assert za.device_status() == za.ZERO_OK
