@@ -74,3 +74,21 @@ def test_our_arm_line():
     for k in ("sm_mhz", "sm_max_mhz", "reasons"):
         assert k in c, k
     assert d["config"]["l2"].startswith("L2 flushed")   # tiny moves less than 4 L2 sizes
+
+
+def test_workload_names():
+    """The bench's workload names: the named configurations, a ZeRO-3 unit (its gather and
+    rank 0's step) and the same unit's step alone."""
+    import bench
+    from synth import configs as C
+    assert bench._workload("1p3b") is C.B1P3
+    assert bench._workload("7b_rank3_prewarm").prewarm == 5
+    u = bench._workload("unit:16777216:8")
+    s = bench._workload("shard:16777216:8")
+    assert u.name.startswith("unit") and not s.name.startswith("unit")
+    for w in (u, s):
+        assert (w.numel, w.world, w.rank, w.grad_layout, w.param_layout) == \
+            (16777216, 8, 0, "shard", "shard")
+        assert w.master_spec() == u.master_spec() and w.grad_spec(3, 2) == u.grad_spec(3, 2)
+    with pytest.raises(SystemExit):
+        bench._workload("nonesuch")
