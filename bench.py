@@ -442,7 +442,7 @@ class Refused(Exception):
     was not updated, so its time is not the time of the step and no line is printed."""
 
 
-def device_verdict(za, dist=None, device=None) -> str:
+def device_state(za, dist=None, device=None) -> str:
     """'ok' if every bounded wait of the library's kernels completed since the last
     check (on every rank), else 'timeout'.  Synchronises the device."""
     bad = 0.0 if za.device_status() == za.ZERO_OK else 1.0
@@ -454,11 +454,11 @@ def device_verdict(za, dist=None, device=None) -> str:
     return "ok" if bad == 0.0 else "timeout"
 
 
-def require_ok(verdict: str, what: str) -> str:
-    if verdict != "ok":
-        raise Refused(f"{what}: a kernel gave up a bounded wait (device status {verdict}); "
+def require_ok(state: str, what: str) -> str:
+    if state != "ok":
+        raise Refused(f"{what}: a kernel gave up a bounded wait (device status {state}); "
                       "the steps did not complete and their time is not reported")
-    return verdict
+    return state
 
 
 def timed_region(rep, stream, steps, t, flush=None, dist=None):
@@ -548,7 +548,7 @@ def run_ours(args, wl):
         t += 1
         rep.step(t, stream)
     torch.cuda.synchronize(dev)
-    require_ok(device_verdict(rep.za, dist, dev), "prewarm and warm-up steps")
+    require_ok(device_state(rep.za, dist, dev), "prewarm and warm-up steps")
 
     nk = len(rep.kernels)
     need = L2Flush.needed(rep.step_bytes(), dev) if args.l2 == "auto" else args.l2 == "flush"
@@ -557,7 +557,7 @@ def run_ours(args, wl):
     sampler.start()
     t, ev, wall = timed_region(rep, stream, args.steps, t, flush, dist)
     clocks = sampler.stop()
-    status = require_ok(device_verdict(rep.za, dist, dev), "timed region")
+    status = require_ok(device_state(rep.za, dist, dev), "timed region")
     if flush is None:
         total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1])
     else:   # the flushes sit between the steps: add up the steps' own launches
@@ -706,7 +706,7 @@ def _e2e(args, rep, stream, t, dist, world_size):
             fn(t)
         e1.record(stream)
         torch.cuda.synchronize(rep.dev)
-        require_ok(device_verdict(rep.za, dist, rep.dev), f"e2e {name} leg")
+        require_ok(device_state(rep.za, dist, rep.dev), f"e2e {name} leg")
         out[name] = aggregate(e0.elapsed_time(e1) / k_steps, rep.unit_elements(), world_size,
                               dist, rep.dev)
     ms, val = out["zero_copy"]
@@ -879,7 +879,7 @@ def run_zero2_buckets(args):
     t_two_graph = timed(graph2.replay)
     t_bwd, t_serial, t_over = timed(backward_only), timed(backward_then_steps), timed(overlapped)
     t_over2 = timed(overlapped_two_streams)
-    status = require_ok(device_verdict(za), "zero2_buckets timed regions")
+    status = require_ok(device_state(za), "zero2_buckets timed regions")
     peak, peak_src = _peaks()
     nbytes = (2 * N + 26) * numel
     line = {
@@ -1000,7 +1000,7 @@ def run_zero3_prefetch(args):
     t_c = timed(lambda: [compute(li, li % 2) for li in range(L)])
     t_ser = timed(serial)
     t_pipe = timed(lambda: prefetch_pass(L, gather, compute, main_s, side))
-    status = require_ok(device_verdict(za), "zero3_prefetch timed regions")
+    status = require_ok(device_state(za), "zero3_prefetch timed regions")
     peak, peak_src = _peaks()
     g_gbs = 4 * U * L / (t_g * 1e-3) / 1e9
     # the library copies on the TMA engine when every tensor offset and row block is a
