@@ -258,3 +258,73 @@ def test_unit_step_withheld_copies_time_out(N):
     torch.cuda.synchronize()
     assert torch.equal(pr.full, torch.cat(pr.shards)[:U])
     assert za.device_status() == za.ZERO_OK
+
+
+@pytest.mark.parametrize("N", [2, 8, 64])
+def test_unit_step_with_host_resident_buffers(N):
+    """The e2e layout: the shards, the gradient slices and the bf16 shard output in pinned
+    host memory (read and written by the kernel over NVLink-C2C; the single launch's bulk
+    copies read the host buffers directly).  The unit and the state must equal the
+    all-device call bit for bit."""
+    U = N * 8 * 4000
+    dev_pr = UnitProblem(U, N, rank=1)
+    host_pr = UnitProblem(U, N, rank=1)
+    for k in range(N):
+        gu.dev_fill_into(dev_pr.g[k][:dev_pr.cnt], dev_pr.wl.grad_spec(k, 1), dev_pr.lo,
+                         synth.OUT_BF16)
+    hs = [torch.empty(dev_pr.S, dtype=torch.int16, pin_memory=True) for _ in range(N)]
+    hg = [torch.empty(dev_pr.S, dtype=torch.int16, pin_memory=True) for _ in range(N)]
+    hp = torch.full((dev_pr.S,), 0x1234, dtype=torch.int16, pin_memory=True)
+    for k in range(N):
+        hs[k].copy_(dev_pr.shards[k])
+        hg[k].copy_(dev_pr.g[k])
+    torch.cuda.synchronize()
+    za.zero3_unit_step(dev_pr.plan, 1, list(dev_pr.shards), dev_pr.full, list(dev_pr.g),
+                       dev_pr.w, dev_pr.m, dev_pr.v, dev_pr.p, lr=1e-3, t=1)
+    za.zero3_unit_step(host_pr.plan, 1, hs, host_pr.full, hg, host_pr.w, host_pr.m, host_pr.v,
+                       hp, lr=1e-3, t=1)
+    torch.cuda.synchronize()
+    assert torch.equal(dev_pr.full, host_pr.full)
+    for a, b in ((dev_pr.w, host_pr.w), (dev_pr.m, host_pr.m), (dev_pr.v, host_pr.v)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(dev_pr.p.cpu(), hp)
+    assert za.device_status() == za.ZERO_OK
+
+
+@pytest.mark.parametrize("N", [2, 8, 64])
+def test_unit_steps_captured_in_a_cuda_graph(N):
+    """Two units' single-launch steps captured into a CUDA graph after their first eager
+    call, replayed, and compared with the same calls made eagerly."""
+    U = N * 8 * 3000
+    a, b = UnitProblem(U, N, rank=0, seed=1), UnitProblem(U, N, rank=N - 1, seed=2)
+    for pr in (a, b):
+        for k in range(N):
+            gu.dev_fill_into(pr.g[k][:pr.cnt], pr.wl.grad_spec(k, 1), pr.lo, synth.OUT_BF16)
+    ea, eb = UnitProblem(U, N, rank=0, seed=1), UnitProblem(U, N, rank=N - 1, seed=2)
+    for pr, src in ((ea, a), (eb, b)):
+        for k in range(N):
+            pr.g[k].copy_(src.g[k])
+
+    def run(prs, t, stream=None):
+        for pr in prs:
+            za.zero3_unit_step(pr.plan, pr.rank, list(pr.shards), pr.full, list(pr.g), pr.w,
+                               pr.m, pr.v, pr.p, lr=1e-3, t=t, stream=stream)
+
+    run((a, b), 1)                          # first calls (per-device set-up) outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run((a, b), 2)
+    graph.replay()
+    torch.cuda.synchronize()
+    for t in (1, 2):
+        run((ea, eb), t)
+    torch.cuda.synchronize()
+    for g_, e_ in ((a, ea), (b, eb)):
+        assert torch.equal(g_.full, e_.full)
+        for x, y in ((g_.w, e_.w), (g_.m, e_.m), (g_.v, e_.v)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+        assert torch.equal(g_.p, e_.p)
+    assert za.device_status() == za.ZERO_OK
