@@ -225,13 +225,12 @@ class Replica:
     def unit_step_kernel_name(self):
         """zero3_unit_step runs the gather and the step as one launch when the shard
         is a multiple of 8 elements, every buffer is 16-byte aligned at its first
-        element and the unit moves at most 512 MiB (256 MiB at N >= 40); otherwise
-        the gather kernel, then the step kernel."""
+        element and the unit moves at most 512 MiB; otherwise the gather kernel, then
+        the step kernel."""
         aligned = all(x.data_ptr() % 16 == 0
                       for x in self.shards + [self.full] + self.g + [self.w, self.m, self.v,
                                                                      self.p])
-        limit = (512 if self.wl.world < 40 else 256) << 20
-        small = 4 * self.wl.numel + _bytes_per_step(self.wl, self.plan) <= limit
+        small = 4 * self.wl.numel + _bytes_per_step(self.wl, self.plan) <= (512 << 20)
         if self.wl.numel >= 8 and self.n >= 8 and self.plan.shard % 8 == 0 and aligned and small:
             return "zero3_unit_step_kernel"
         return f"{self.gather_kernel_name()}+{self.step_kernel_name()}"

@@ -266,8 +266,7 @@ int zero3_unit_gather_rows(int32_t ntensors, const int64_t* rows, const int64_t*
  * When the shard is a multiple of 8 elements, every buffer of both parts is
  * 16-byte aligned at its first element, the gradients are bf16, the sum is
  * fp32 and the unit moves at most 512 MiB (gather 4 bytes per unit element +
- * step (2*world + 26) bytes per stepped element; 256 MiB at world >= 40), the
- * single launch runs (bulk copies on the TMA engine, bounded waits reported by
+ * step (2*world + 26) bytes per stepped element), the single launch runs (bulk copies on the TMA engine, bounded waits reported by
  * zero_device_status); otherwise the two kernels are launched in order on the
  * stream (larger units stream as fast that way, with the launch cost
  * amortised).  Errors: those of zero3_unit_gather and

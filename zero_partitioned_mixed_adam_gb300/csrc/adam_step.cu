@@ -876,13 +876,11 @@ cudaError_t launch_variant(const StepLaunch& L) {
 // Measured on GB300 against the gather and the step as two launches, units
 // of 2^22..2^27 elements with the L2 flushed: at N = 2 and 8 the single launch
 // takes 0.71-0.87 of the time up to 320 MB and 0.95-0.98 at 620 MB, and
-// 1.01-1.03 at 1.2 GB; at N = 64 (two gather slots beside the larger step
-// ring) 0.62-0.96 up to 215 MB and 1.14 at 430 MB.  Past these sizes each
-// kernel alone streams at its own best and the launch cost is amortised,
-// while inside the single launch the gather's ring falls behind the step's
-// consumers and finishes alone.
+// 1.01-1.03 at 1.2 GB; at N = 32 and 64 0.65-0.81 up to 460 MB.  Past these
+// sizes each kernel alone streams at its own best and the launch cost is
+// amortised, while inside the single launch the gather's ring falls behind
+// the step's consumers and finishes alone.
 constexpr int64_t kFusedMaxBytes = int64_t{512} << 20;
-constexpr int64_t kFusedMaxBytesLargeN = int64_t{256} << 20;
 
 // The fused unit step when both parts can run on the TMA engine: the gather's
 // shard a multiple of 8 elements, and every buffer of both parts 16-byte
@@ -891,17 +889,20 @@ constexpr int64_t kFusedMaxBytesLargeN = int64_t{256} << 20;
 bool launch_unit_step_fused(const GatherLaunch& GL, const StepLaunch& L, cudaError_t* err) {
   if (L.grad_f32 || L.acc_bf16 || L.n < 8 || GL.numel < 8 || GL.shard % 8 != 0) return false;
   const int64_t bytes = 4 * GL.numel + (2 * static_cast<int64_t>(L.world) + 26) * L.n;
-  if (bytes > (L.world < 40 ? kFusedMaxBytes : kFusedMaxBytesLargeN)) return false;
+  if (bytes > kFusedMaxBytes) return false;
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   bool ok = a16(GL.full) && a16(L.master) && a16(L.m) && a16(L.v) && a16(L.param);
   for (int k = 0; k < GL.world && ok; ++k) ok = a16(GL.shards[k]);
   for (int k = 0; k < L.world && ok; ++k) ok = a16(L.grads[k]);
   if (!ok) return false;
   const int64_t nbody = L.n & ~static_cast<int64_t>(7);
+  // N >= 24: a two-stage step ring leaves room for four gather slots (measured
+  // against three stages and two slots: 2^24-element units at N = 64 0.0146 vs
+  // 0.0209 ms, at N = 32 0.0154 vs 0.0168 with the N < 24 shape).
   if (L.world <= 4) return launch_unit_step_shape<1, 8, 24, 1, 4, 64, true>(GL, L, nbody, err);
-  if (L.world < 40) return launch_unit_step_shape<8, 4, 22, 3, 4, 64, false>(GL, L, nbody, err);
-  if (L.world <= 64) return launch_unit_step_shape<32, 2, 16, 3, 2, 64, false>(GL, L, nbody, err);
-  return launch_unit_step_shape<32, 2, 16, 3, 2, kTableRuntime, false>(GL, L, nbody, err);
+  if (L.world < 24) return launch_unit_step_shape<8, 4, 22, 3, 4, 64, false>(GL, L, nbody, err);
+  if (L.world <= 64) return launch_unit_step_shape<32, 2, 16, 2, 4, 64, false>(GL, L, nbody, err);
+  return launch_unit_step_shape<32, 2, 16, 2, 4, kTableRuntime, false>(GL, L, nbody, err);
 }
 
 }  // namespace
