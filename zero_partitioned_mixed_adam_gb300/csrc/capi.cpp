@@ -132,14 +132,17 @@ Range bytes_of(const void* p, int64_t first, int64_t count, int esize) {
   const uintptr_t b = reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(first) * esize;
   return {b, b + static_cast<uintptr_t>(count) * esize};
 }
+bool nonempty(Range r) { return r.hi > r.lo; }
 
 // A step over [begin, end), checked: its launch and the byte ranges it
 // touches (for the unit step's checks across its two parts).
 struct PreparedStep {
   StepLaunch L;
-  const void* g[ZERO_MAX_WORLD];    // gradient pointers at the range's first element
-  Range outs[4];                    // master, m, v, param bytes written (L.n > 0)
-  Range grads[ZERO_MAX_WORLD];      // gradient bytes read (L.n > 0)
+  const void* g[ZERO_MAX_WORLD];  // gradient pointers at the range's first element
+  Range outs[4];                  // master, m, v, param bytes written (L.n > 0)
+  int gsize;                      // bytes per gradient element
+  // gradient k's bytes read (L.n > 0)
+  Range grad_bytes(int32_t k) const { return bytes_of(g[k], 0, L.n, gsize); }
 };
 
 // The checks of one step over [begin, end) (every step entry point).
@@ -207,15 +210,16 @@ int prepare_step(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t e
       for (int j = i + 1; j < 4; ++j)
         if (overlap(ps->outs[i], ps->outs[j])) return ZERO_E_ALIAS;
     for (int32_t k = 0; k < N; ++k) {
-      ps->grads[k] = bytes_of(grad_ptrs[k], g_first, n, gsize);
+      const Range gk = bytes_of(grad_ptrs[k], g_first, n, gsize);
       for (int i = 0; i < 4; ++i)
-        if (overlap(ps->grads[k], ps->outs[i])) return ZERO_E_ALIAS;
+        if (overlap(gk, ps->outs[i])) return ZERO_E_ALIAS;
     }
   }
 
   // Offset every pointer to the range's first element.
   for (int32_t k = 0; k < N; ++k)
     ps->g[k] = static_cast<const char*>(grad_ptrs[k]) + g_first * gsize;
+  ps->gsize = gsize;
 
   StepLaunch& L = ps->L;
   L.grads = ps->g;
@@ -247,8 +251,14 @@ int prepare_step(const zero_plan_t* plan, int32_t rank, int64_t begin, int64_t e
 // A flat unit gather, checked: its launch and the byte ranges it touches.
 struct PreparedGather {
   GatherLaunch L;
-  Range out;                         // the unit's bytes written
-  Range shards[ZERO_MAX_WORLD];      // the shards' bytes read
+  Range out;  // the unit's bytes written
+  // shard k's bytes read (empty for a shard that holds only padding)
+  Range shard_bytes(int32_t k) const {
+    int64_t cnt = L.numel - static_cast<int64_t>(k) * L.shard;
+    if (cnt > L.shard) cnt = L.shard;
+    if (cnt < 0) cnt = 0;
+    return bytes_of(L.shards[k], 0, cnt, 2);
+  }
 };
 
 int prepare_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs, void* full_bf16,
@@ -262,14 +272,6 @@ int prepare_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs, 
   if (reinterpret_cast<uintptr_t>(full_bf16) & 1u) return ZERO_E_ALIGN;
   for (int32_t k = 0; k < N; ++k)
     if (reinterpret_cast<uintptr_t>(shard_ptrs[k]) & 1u) return ZERO_E_ALIGN;
-  pg->out = bytes_of(full_bf16, 0, unit_plan->numel, 2);
-  for (int32_t k = 0; k < N; ++k) {
-    int64_t cnt = unit_plan->numel - static_cast<int64_t>(k) * unit_plan->shard;
-    if (cnt > unit_plan->shard) cnt = unit_plan->shard;
-    if (cnt < 0) cnt = 0;
-    pg->shards[k] = bytes_of(shard_ptrs[k], 0, cnt, 2);
-    if (cnt > 0 && overlap(pg->out, pg->shards[k])) return ZERO_E_ALIAS;
-  }
   GatherLaunch& L = pg->L;
   L.shards = reinterpret_cast<const uint16_t* const*>(shard_ptrs);
   L.world = N;
@@ -278,10 +280,13 @@ int prepare_gather(const zero_plan_t* unit_plan, const void* const* shard_ptrs, 
   L.shard = unit_plan->shard;
   L.stream = static_cast<cudaStream_t>(stream);
   L.withhold = g_withhold.load(std::memory_order_relaxed);
+  pg->out = bytes_of(full_bf16, 0, unit_plan->numel, 2);
+  for (int32_t k = 0; k < N; ++k) {
+    const Range sk = pg->shard_bytes(k);
+    if (nonempty(sk) && overlap(pg->out, sk)) return ZERO_E_ALIAS;
+  }
   return ZERO_OK;
 }
-
-bool nonempty(Range r) { return r.hi > r.lo; }
 
 }  // namespace
 }  // namespace zeroadam
@@ -337,13 +342,14 @@ int zero3_unit_step(const zero_plan_t* unit_plan, int32_t rank, const void* cons
   // the step reads or writes, and the shards must not overlap what it writes.
   if (ps.L.n > 0) {
     const int32_t N = static_cast<int32_t>(unit_plan->world);
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 4; ++i)
       if (overlap(pg.out, ps.outs[i])) return ZERO_E_ALIAS;
-      for (int32_t k = 0; k < N; ++k)
-        if (nonempty(pg.shards[k]) && overlap(pg.shards[k], ps.outs[i])) return ZERO_E_ALIAS;
+    for (int32_t k = 0; k < N; ++k) {
+      const Range sk = pg.shard_bytes(k);
+      for (int i = 0; i < 4; ++i)
+        if (nonempty(sk) && overlap(sk, ps.outs[i])) return ZERO_E_ALIAS;
+      if (overlap(pg.out, ps.grad_bytes(k))) return ZERO_E_ALIAS;
     }
-    for (int32_t k = 0; k < N; ++k)
-      if (overlap(pg.out, ps.grads[k])) return ZERO_E_ALIAS;
   }
   return launch_status(launch_unit_step(pg.L, ps.L));
 }
