@@ -25,6 +25,8 @@ CHILD = textwrap.dedent("""
         lib.zero3_unit_gather(None, None, None, None),
         lib.zero3_unit_gather_rows(0, None, None, 1, None, None, None),
         lib.zero_device_status(),   # ZERO_E_DEVICE without a GPU, ZERO_OK with one
+        lib.zero3_unit_step(None, 0, None, None, None, 1, None, None, None, None, 1,
+                            1e-3, 0.9, 0.999, 1e-8, 1, None),
     ]
     plan = za.ZeroPlan()
     codes.append(lib.zero_plan(1000, 4, ctypes.byref(plan)))   # host only: not traced
@@ -55,9 +57,10 @@ def test_entry_points_open_and_close_their_ranges(tracer_so):
     c = codes.split(",")
     assert c[:4] == [str(e["ZERO_E_NULLPTR"]), str(e["ZERO_E_NULLPTR"]),
                      str(e["ZERO_E_NULLPTR"]), str(e["ZERO_E_SHAPE"])]
-    assert c[4] in ("0", str(e["ZERO_E_DEVICE"])) and c[5] == "0"
+    assert c[4] in ("0", str(e["ZERO_E_DEVICE"])) and c[5] == str(e["ZERO_E_NULLPTR"])
+    assert c[6] == "0"
     assert log == ("+zero_adam_step;-;+zero_adam_step_range;-;+zero3_unit_gather;-;"
-                   "+zero3_unit_gather_rows;-;+zero_device_status;-;")
+                   "+zero3_unit_gather_rows;-;+zero_device_status;-;+zero3_unit_step;-;")
 
 
 def test_no_tool_attached_costs_nothing_visible(tracer_so):
