@@ -92,3 +92,23 @@ def test_workload_names():
         assert w.master_spec() == u.master_spec() and w.grad_spec(3, 2) == u.grad_spec(3, 2)
     with pytest.raises(SystemExit):
         bench._workload("nonesuch")
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")
+@pytest.mark.parametrize("mode", ["fused", "separate"])
+def test_unit_workload_line(mode):
+    """A ZeRO-3 unit workload's line: one zero3_unit_step call per step (one launch for a
+    unit this small) or the gather and the step as two calls; the roofline names the
+    dominant launch and the device status is clear."""
+    d = _line("--workload", "unit:1048576:8", "--unit-mode", mode, "--steps", "3", "--warmup",
+              "3", "--no-e2e", "--no-cpu-baseline")
+    assert d["config"]["workload"] == "unit1048576_n8" and d["device_status"] == "ok"
+    assert d["value"] > 0 and d["roofline"]["bound"] == "hbm"
+    names = [k["kernel"] for k in d["kernels"]]
+    if mode == "fused":
+        assert names == ["zero3_unit_step_kernel"] and d["gpu_launches"] == 3
+    else:
+        assert names == ["zero3_unit_gather_tma_kernel", "zero_adam_step_tma_grad_kernel"]
+        assert d["gpu_launches"] == 6
+    assert d["config"]["bytes_per_step"] == 4 * 1048576 + (2 * 8 + 26) * 131072
