@@ -63,9 +63,14 @@ def _workload(name):
 
 
 def _bytes_per_step(wl, plan):
-    """Algorithmic bytes of one step: (2N + 26) per stepped element."""
+    """Algorithmic bytes of one step: (2N + 26) per stepped element ((4N + 26) with fp32
+    gradients)."""
     n = _elements(wl, plan)
-    return (2 * wl.world + 26) * n
+    return ((4 if wl.grad_f32 else 2) * wl.world + 26) * n
+
+
+def _grad_flags(za, wl):
+    return (za.ZERO_GRAD_F32 if wl.grad_f32 else 0) | (za.ZERO_ACC_BF16 if wl.acc_bf16 else 0)
 
 
 def _elements(wl, plan):
@@ -190,7 +195,8 @@ class Replica:
         p_len = S if wl.param_layout == "shard" else wl.numel
         self.g_first = 0 if wl.grad_layout == "shard" else self.lo
         self.p_first = 0 if wl.param_layout == "shard" else self.lo
-        self.g = [torch.zeros(g_len, dtype=torch.int16, device=dev) for _ in range(wl.world)]
+        gdt = torch.float32 if wl.grad_f32 else torch.int16
+        self.g = [torch.zeros(g_len, dtype=gdt, device=dev) for _ in range(wl.world)]
         self.w = torch.zeros(s_len, dtype=torch.float32, device=dev)
         self.m = torch.zeros_like(self.w)
         self.v = torch.zeros_like(self.w)
@@ -231,7 +237,9 @@ class Replica:
                       for x in self.shards + [self.full] + self.g + [self.w, self.m, self.v,
                                                                      self.p])
         small = 4 * self.wl.numel + _bytes_per_step(self.wl, self.plan) <= (512 << 20)
-        if self.wl.numel >= 8 and self.n >= 8 and self.plan.shard % 8 == 0 and aligned and small:
+        plain = not (self.wl.grad_f32 or self.wl.acc_bf16)
+        if (self.wl.numel >= 8 and self.n >= 8 and self.plan.shard % 8 == 0 and aligned and small
+                and plain):
             return "zero3_unit_step_kernel"
         return f"{self.gather_kernel_name()}+{self.step_kernel_name()}"
 
@@ -241,8 +249,9 @@ class Replica:
         element (whole cudaMalloc buffers); the register-staged kernel otherwise."""
         def aligned(t, first, esize):
             return (t.data_ptr() + first * esize) % 16 == 0
-        tma = (self.wl.world >= 5 and self.n >= 8
-               and all(aligned(g, self.g_first, 2) for g in self.g)
+        gsize = 4 if self.wl.grad_f32 else 2
+        tma = (self.wl.world >= 5 and self.n >= 8 and not self.wl.grad_f32 and not self.wl.acc_bf16
+               and all(aligned(g, self.g_first, gsize) for g in self.g)
                and all(aligned(x, 0, 4) for x in (self.w, self.m, self.v))
                and aligned(self.p, self.p_first, 2))
         return "zero_adam_step_tma_grad_kernel" if tma else "zero_adam_step_kernel"
@@ -251,9 +260,10 @@ class Replica:
         import torch
         import synth
         st = torch.cuda.current_stream(self.dev).cuda_stream
+        kind, gsize = (synth.OUT_F32, 4) if self.wl.grad_f32 else (synth.OUT_BF16, 2)
         for k in range(self.wl.world):
-            synth.fill_dev(self.wl.grad_spec(k, t), self.lo, self.n, synth.OUT_BF16,
-                           self.g[k].data_ptr() + 2 * self.g_first, st)
+            synth.fill_dev(self.wl.grad_spec(k, t), self.lo, self.n, kind,
+                           self.g[k].data_ptr() + gsize * self.g_first, st)
 
     def step(self, t, stream, ev=None, grads=None, shards=None, param=None):
         """Issue one step; ev[i] = (start, end) events around launch i when given.
@@ -267,7 +277,8 @@ class Replica:
                                grads or self.g, self.w, self.m, self.v,
                                param if param is not None else self.p, lr=wl.lr,
                                beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, t=t,
-                               grad_layout=za.ZERO_GRAD_SHARD, param_layout=za.ZERO_PARAM_SHARD,
+                               grad_layout=za.ZERO_GRAD_SHARD | _grad_flags(za, wl),
+                               param_layout=za.ZERO_PARAM_SHARD,
                                stream=stream)
             if ev is not None:
                 ev[0][1].record(stream)
@@ -284,7 +295,8 @@ class Replica:
         za.zero_adam_step(self.plan, wl.rank, grads or self.g, self.w, self.m, self.v,
                           param if param is not None else self.p, lr=wl.lr, beta1=wl.beta1,
                           beta2=wl.beta2, eps=wl.eps, t=t,
-                          grad_layout=za.ZERO_GRAD_SHARD if wl.grad_layout == "shard" else 0,
+                          grad_layout=(za.ZERO_GRAD_SHARD if wl.grad_layout == "shard" else 0)
+                          | _grad_flags(za, wl),
                           param_layout=za.ZERO_PARAM_SHARD if wl.param_layout == "shard" else 0,
                           stream=stream)
         if ev is not None:
@@ -335,7 +347,8 @@ class OracleSample:
         lo = wl.rank * S if wl.rank >= 0 else 0
         n = min(max_elems, wl.numel - lo, S if wl.rank >= 0 else wl.numel)
         self.a, self.b, self.n = lo, lo + n, n
-        self.grads = [synth.fill_host(wl.grad_spec(k, wl.prewarm + 1), lo, n, synth.OUT_BF16)
+        kind = synth.OUT_F32 if wl.grad_f32 else synth.OUT_BF16
+        self.grads = [synth.fill_host(wl.grad_spec(k, wl.prewarm + 1), lo, n, kind)
                       for k in range(wl.world)]
         self.hw = synth.fill_host(wl.master_spec(), lo, n, synth.OUT_F32)
         self.hm = np.zeros(n, np.float32)
@@ -357,7 +370,8 @@ class OracleSample:
             oracle.zero_step(wl.numel, wl.world, -1 if wl.rank < 0 else wl.rank, self.grads,
                              self.hw, self.hm, self.hv, self.hp, wl.lr, wl.beta1, wl.beta2,
                              wl.eps, t, i0=ab[0], i1=ab[1], grad_base=a, state_base=a,
-                             param_base=a)
+                             param_base=a, grad_f32=wl.grad_f32,
+                             acc_bf16=wl.acc_bf16)
         with ThreadPoolExecutor(max_workers=self.cores) as ex:
             list(ex.map(run, self.bounds))
 
@@ -382,7 +396,8 @@ class OracleSample:
             oracle.zero_step(wl.numel, wl.world, -1 if wl.rank < 0 else wl.rank, self.grads,
                              self.hw, self.hm, self.hv, self.hp, wl.lr, wl.beta1, wl.beta2,
                              wl.eps, self.t, i0=a, i1=a + n, grad_base=a, state_base=a,
-                             param_base=a)
+                             param_base=a, grad_f32=wl.grad_f32,
+                             acc_bf16=wl.acc_bf16)
             done += n
             el = time.perf_counter() - t0
             if el >= seconds:
@@ -507,7 +522,9 @@ def _config(wl, rep, flush=None):
          "rank": "all" if wl.rank < 0 else wl.rank, "grad_layout": wl.grad_layout,
          "param_layout": wl.param_layout, "grad_dist": ["normal", "student_t3"][wl.grad_dist],
          "l2": l2, "parallelism": "replicas",
-         "state": "fp32 master/m/v, bf16 grads and params"}
+         "state": "fp32 master/m/v, bf16 params",
+         "gradients": "fp32" if wl.grad_f32 else "bf16",
+         "reduce": "bf16-rounded sum" if wl.acc_bf16 else "fp32 sum"}
     if rep is not None:
         c["shard"] = rep.plan.shard
         c["bytes_per_step"] = rep.step_bytes()
@@ -645,9 +662,10 @@ def _e2e(args, rep, stream, t, dist, world_size):
     wl = rep.wl
     k_steps = max(1, min(args.steps, args.e2e_steps))
     n = rep.n
+    gsize = 4 if wl.grad_f32 else 2
     g_len = rep.g[0].numel()
     # every rank on this host pins its own copy: keep the total within half of what is free
-    need = 2 * g_len * wl.world + 2 * rep.p.numel()
+    need = gsize * g_len * wl.world + 2 * rep.p.numel()
     if rep.unit:
         need += sum(2 * x.numel() for x in rep.shards)
     local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
@@ -658,11 +676,11 @@ def _e2e(args, rep, stream, t, dist, world_size):
         dist.all_reduce(flag, op=dist.ReduceOp.MAX)
         skip = flag.item() > 0
     if skip:
-        return {"value": None, "unit": "Gelem/s", "h2d_bytes_per_step": 2 * n * wl.world,
+        return {"value": None, "unit": "Gelem/s", "h2d_bytes_per_step": gsize * n * wl.world,
                 "d2h_bytes_per_step": 2 * n, "skipped": (
                     f"{local_ranks} ranks x {need / 1e9:.1f} GB of pinned host buffers exceed half "
                     f"of the host memory available"), "_steps": 0}
-    hg = [torch.empty(g_len, dtype=torch.int16, pin_memory=True) for _ in range(wl.world)]
+    hg = [torch.empty(g_len, dtype=rep.g[0].dtype, pin_memory=True) for _ in range(wl.world)]
     for k in range(wl.world):
         hg[k].copy_(rep.g[k])
     hs = None
@@ -672,11 +690,11 @@ def _e2e(args, rep, stream, t, dist, world_size):
             hsk.copy_(sk)
     hp = torch.empty(rep.p.numel(), dtype=torch.int16, pin_memory=True)
     torch.cuda.synchronize(rep.dev)
-    in_bytes = sum(x.numel() * 2 for x in hg)
+    in_bytes = sum(x.numel() * gsize for x in hg)
     if rep.unit:
-        in_bytes = 2 * n * wl.world + sum(x.numel() * 2 for x in hs)
+        in_bytes = gsize * n * wl.world + sum(x.numel() * 2 for x in hs)
     elif wl.grad_layout != "shard":
-        in_bytes = 2 * n * wl.world   # the kernel reads the stepped range only
+        in_bytes = gsize * n * wl.world   # the kernel reads the stepped range only
 
     def zero_copy(tt):
         rep.step(tt, stream, grads=hg, shards=hs, param=hp)
@@ -1056,6 +1074,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=8, help="zero3_prefetch: units per pass")
     ap.add_argument("--prefetch-world", type=int, default=8, help="zero3_prefetch: ranks")
     ap.add_argument("--tokens", type=int, default=4096, help="zero3_prefetch: GEMM rows")
+    ap.add_argument("--grad-variant", choices=("bf16", "f32", "bf16sum"), default="bf16",
+                    help="gradients in bf16 (the method), fp32 (the page's runnable demo), or "
+                         "bf16 with the sum over ranks rounded to bf16 after every addition")
     ap.add_argument("--l2", choices=("auto", "flush", "none"), default="auto",
                     help="flush the L2 before every timed step: auto = when a step moves less "
                          "than four L2 sizes")
@@ -1073,9 +1094,13 @@ def main(argv=None):
         if args.workload == "zero2_buckets":
             return run_zero2_buckets(args)
         wl = _workload(args.workload)
+        import dataclasses
         if args.numel:
-            import dataclasses
             wl = dataclasses.replace(wl, numel=args.numel, name=f"{wl.name}@numel={args.numel}")
+        if args.grad_variant != "bf16":
+            wl = dataclasses.replace(wl, grad_f32=args.grad_variant == "f32",
+                                     acc_bf16=args.grad_variant == "bf16sum",
+                                     name=f"{wl.name}+{args.grad_variant}")
         if args.impl == "reference":
             return run_reference(args, wl)
         return run_ours(args, wl)

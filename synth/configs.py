@@ -66,6 +66,8 @@ class StepWorkload:
     outlier_value: float = 0.0
     master_sigma: float = 0.02
     shapes: tuple = field(default=())
+    grad_f32: bool = False      # gradient buffers hold fp32 (the page's runnable demo)
+    acc_bf16: bool = False      # the sum over ranks is rounded to bf16 after every addition
 
     @property
     def shard(self) -> int:

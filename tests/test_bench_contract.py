@@ -112,3 +112,13 @@ def test_unit_workload_line(mode):
         assert names == ["zero3_unit_gather_tma_kernel", "zero_adam_step_tma_grad_kernel"]
         assert d["gpu_launches"] == 6
     assert d["config"]["bytes_per_step"] == 4 * 1048576 + (2 * 8 + 26) * 131072
+
+
+@pytest.mark.parametrize("variant,grads,reduce", [("f32", "fp32", "fp32 sum"),
+                                                  ("bf16sum", "bf16", "bf16-rounded sum")])
+def test_reference_arm_gradient_variants(variant, grads, reduce):
+    """The f4 variants reach the oracle: the reference arm steps the same variant."""
+    d = _line("--impl", "reference", "--workload", "tiny", "--grad-variant", variant,
+              "--steps", "1", "--warmup", "3")
+    assert d["config"]["gradients"] == grads and d["config"]["reduce"] == reduce
+    assert d["config"]["workload"] == f"tiny+{variant}" and d["value"] > 0
