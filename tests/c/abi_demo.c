@@ -7,6 +7,11 @@
  *                     buffers, zero gradients and m = v = 0, where Adam leaves
  *                     the master weights unchanged and the bf16 parameters are
  *                     their round-to-nearest-even cast.
+ *   abi_demo unit   : one ZeRO-3 unit step (gather + one rank's step in one
+ *                     call) on 8 ranks' shards: the gathered unit is the
+ *                     shards back to back, bit for bit, and the rank's step
+ *                     under a zero gradient behaves as above; the device
+ *                     status afterwards is ZERO_OK.
  * Exit status 0 on success.
  */
 #include <cuda_runtime_api.h>
@@ -89,7 +94,63 @@ static int step_check(void) {
   return 0;
 }
 
+static int unit_check(void) {
+  const int64_t numel = 1000000;
+  const int32_t world = 8, rank = 5;
+  zero_plan_t p;
+  if (zero_plan(numel, world, &p) != ZERO_OK) return fail("zero_plan");
+  const size_t S = (size_t)p.shard;
+  uint16_t* hs = (uint16_t*)malloc(S * 2);
+  float* hw = (float*)malloc(S * 4);
+  void* shards[8];
+  void* grads[8];
+  for (int r = 0; r < world; ++r) {
+    for (size_t j = 0; j < S; ++j) hs[j] = (uint16_t)(0x3c00u + ((uint32_t)r * 977u + (uint32_t)j) % 4093u);
+    if (cudaMalloc(&shards[r], S * 2) != cudaSuccess) return fail("cudaMalloc");
+    cudaMemcpy(shards[r], hs, S * 2, cudaMemcpyHostToDevice);
+    if (cudaMalloc(&grads[r], S * 2) != cudaSuccess) return fail("cudaMalloc");
+    cudaMemset(grads[r], 0, S * 2);
+  }
+  for (size_t j = 0; j < S; ++j) hw[j] = 0.003f * (float)((int)(j % 211) - 105);
+  void* full;
+  float *w, *m, *v;
+  uint16_t* par;
+  cudaMalloc(&full, (size_t)numel * 2);
+  cudaMalloc((void**)&w, S * 4);
+  cudaMalloc((void**)&m, S * 4);
+  cudaMalloc((void**)&v, S * 4);
+  cudaMalloc((void**)&par, S * 2);
+  cudaMemcpy(w, hw, S * 4, cudaMemcpyHostToDevice);
+  cudaMemset(m, 0, S * 4);
+  cudaMemset(v, 0, S * 4);
+  cudaMemset(full, 0xff, (size_t)numel * 2);
+  const int rc = zero3_unit_step(&p, rank, (const void* const*)shards, full,
+                                 (const void* const*)grads, ZERO_GRAD_SHARD, w, m, v, par,
+                                 ZERO_PARAM_SHARD, 1e-3, 0.9, 0.999, 1e-8, 1, NULL);
+  if (rc != ZERO_OK) return fail(zero_strerror(rc));
+  const int st = zero_device_status();
+  if (st != ZERO_OK) return fail(zero_strerror(st));
+  uint16_t* hf = (uint16_t*)malloc((size_t)numel * 2);
+  float* w2 = (float*)malloc(S * 4);
+  uint16_t* p2 = (uint16_t*)malloc(S * 2);
+  cudaMemcpy(hf, full, (size_t)numel * 2, cudaMemcpyDeviceToHost);
+  cudaMemcpy(w2, w, S * 4, cudaMemcpyDeviceToHost);
+  cudaMemcpy(p2, par, S * 2, cudaMemcpyDeviceToHost);
+  for (int64_t i = 0; i < numel; ++i) {
+    const uint32_t r = (uint32_t)(i / (int64_t)S), j = (uint32_t)(i % (int64_t)S);
+    if (hf[i] != (uint16_t)(0x3c00u + (r * 977u + j) % 4093u)) return fail("gathered unit differs");
+  }
+  for (size_t j = 0; j < S; ++j) {
+    if (memcmp(&w2[j], &hw[j], 4) != 0) return fail("master changed under a zero gradient");
+    if (p2[j] != bf16_rne(hw[j])) return fail("bf16 shard is not the cast of the master");
+  }
+  printf("unit ok: %lld-element unit gathered from %d shards, rank %d stepped, status ok\n",
+         (long long)numel, world, rank);
+  return 0;
+}
+
 int main(int argc, char** argv) {
   if (argc > 1 && strcmp(argv[1], "step") == 0) return step_check();
+  if (argc > 1 && strcmp(argv[1], "unit") == 0) return unit_check();
   return plan_checks();
 }

@@ -35,3 +35,11 @@ def test_c_program_runs_a_step(demo):
     r = subprocess.run([demo, "step"], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert "step ok" in r.stdout
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")
+def test_c_program_runs_a_unit_step(demo):
+    r = subprocess.run([demo, "unit"], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "unit ok" in r.stdout
