@@ -104,7 +104,12 @@ class ClockSampler:
             return
         self.t = threading.Thread(target=self._read, daemon=True)
         self.t.start()
-        time.sleep(0.3)
+        # return once the first sample is in (nvidia-smi attached and querying), so that
+        # the steps that follow are sampled from their start
+        deadline = time.perf_counter() + 10.0
+        while not self.lines and time.perf_counter() < deadline and self.proc.poll() is None:
+            time.sleep(0.01)
+        time.sleep(0.1)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -560,19 +565,27 @@ def run_ours(args, wl):
         rep.fill_grads(t)
         rep.step(t, stream)
     rep.fill_grads(wl.prewarm + 1)
-    for _ in range(args.warmup):
-        t += 1
-        rep.step(t, stream)
-    torch.cuda.synchronize(dev)
-    require_ok(device_state(rep.za, dist, dev), "prewarm and warm-up steps")
 
     nk = len(rep.kernels)
     need = L2Flush.needed(rep.step_bytes(), dev) if args.l2 == "auto" else args.l2 == "flush"
     flush = L2Flush(dev) if need else None
+    # The clock sampler starts before the warm-up steps, which run as the timed steps do
+    # (with the flush) and lead straight into the timed region: a GPU left idle while
+    # nvidia-smi starts lowers its clocks, and the first launch after such a pause ran
+    # up to twice its usual time.
     sampler = ClockSampler(local)
     sampler.start()
-    t, ev, wall = timed_region(rep, stream, args.steps, t, flush, dist)
-    clocks = sampler.stop()
+    try:
+        for i in range(args.warmup):
+            t += 1
+            if flush is not None:
+                flush(i)
+            rep.step(t, stream)
+        torch.cuda.synchronize(dev)
+        require_ok(device_state(rep.za, dist, dev), "prewarm and warm-up steps")
+        t, ev, wall = timed_region(rep, stream, args.steps, t, flush, dist)
+    finally:
+        clocks = sampler.stop()
     status = require_ok(device_state(rep.za, dist, dev), "timed region")
     if flush is None:
         total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1])
