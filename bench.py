@@ -202,6 +202,7 @@ class Replica:
         self.p_first = 0 if wl.param_layout == "shard" else self.lo
         gdt = torch.float32 if wl.grad_f32 else torch.int16
         self.g = [torch.zeros(g_len, dtype=gdt, device=dev) for _ in range(wl.world)]
+        self.g_ptrs = za.pointer_array(self.g)
         self.w = torch.zeros(s_len, dtype=torch.float32, device=dev)
         self.m = torch.zeros_like(self.w)
         self.v = torch.zeros_like(self.w)
@@ -216,6 +217,7 @@ class Replica:
                 synth.fill_dev(C.unit_shard_spec(wl.numel, wl.world, r), 0, S, synth.OUT_BF16,
                                self.shards[r].data_ptr(), st)
             self.full = torch.empty(wl.numel, dtype=torch.int16, device=dev)
+            self.shard_ptrs = za.pointer_array(self.shards)
         # (name, algorithmic bytes) of the step's timed calls, in order
         self.kernels = []
         if self.unit and self.unit_mode == "fused":
@@ -278,8 +280,10 @@ class Replica:
         if self.unit and self.unit_mode == "fused":
             if ev is not None:
                 ev[0][0].record(stream)
-            za.zero3_unit_step(self.plan, wl.rank, shards or self.shards, self.full,
-                               grads or self.g, self.w, self.m, self.v,
+            za.zero3_unit_step(self.plan, wl.rank,
+                               shards if shards is not None else self.shard_ptrs, self.full,
+                               grads if grads is not None else self.g_ptrs,
+                               self.w, self.m, self.v,
                                param if param is not None else self.p, lr=wl.lr,
                                beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, t=t,
                                grad_layout=za.ZERO_GRAD_SHARD | _grad_flags(za, wl),
@@ -291,13 +295,15 @@ class Replica:
         if self.unit:
             if ev is not None:
                 ev[i][0].record(stream)
-            za.zero3_unit_gather(self.plan, shards or self.shards, self.full, stream=stream)
+            za.zero3_unit_gather(self.plan, shards if shards is not None else self.shard_ptrs,
+                                 self.full, stream=stream)
             if ev is not None:
                 ev[i][1].record(stream)
             i += 1
         if ev is not None:
             ev[i][0].record(stream)
-        za.zero_adam_step(self.plan, wl.rank, grads or self.g, self.w, self.m, self.v,
+        za.zero_adam_step(self.plan, wl.rank, grads if grads is not None else self.g_ptrs,
+                          self.w, self.m, self.v,
                           param if param is not None else self.p, lr=wl.lr, beta1=wl.beta1,
                           beta2=wl.beta2, eps=wl.eps, t=t,
                           grad_layout=(za.ZERO_GRAD_SHARD if wl.grad_layout == "shard" else 0)

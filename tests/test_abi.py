@@ -160,6 +160,31 @@ def test_step_argument_errors(za):
     assert _step(za, empty, rank=3, layout=1, player=1) == 0
 
 
+def test_pointer_array_is_marshalled_once(za):
+    """A PointerArray carries the C array of addresses built when it was made; the calls
+    pass that array itself, and check its length against the plan like a list's."""
+    addrs = [BASE + 5 * 2**30 + k * 2**28 for k in range(4)]
+    pa = za.pointer_array(addrs)
+    assert len(pa) == 4 and list(pa.buffers) == addrs
+    assert za._ptrs(pa) is pa.arr
+    assert [pa.arr[k] for k in range(4)] == addrs
+    fresh = za._ptrs(addrs)
+    assert fresh is not pa.arr and [fresh[k] for k in range(4)] == addrs
+    plan = za.zero_plan(1000, 4)
+    kw = dict(lr=1e-3, t=0)
+    # t = 0 is refused before any CUDA call: the same error through a list and the array
+    for grads in (addrs, pa):
+        with pytest.raises(za.ZeroError) as e:
+            za.zero_adam_step(plan, -1, grads, BASE + 2**30, BASE + 2 * 2**30, BASE + 3 * 2**30,
+                              BASE + 4 * 2**30, **kw)
+        assert e.value.code == "ZERO_E_STEP"
+    with pytest.raises(ValueError):
+        za.zero_adam_step(za.zero_plan(1000, 3), -1, pa, BASE + 2**30, BASE + 2 * 2**30,
+                          BASE + 3 * 2**30, BASE + 4 * 2**30, **kw)
+    with pytest.raises(ValueError):
+        za.zero3_unit_gather(za.zero_plan(1000, 2), pa, BASE + 2**30)
+
+
 def test_range_argument_errors(za):
     plan = za.zero_plan(1000, 4)
     lib = za.raw_lib()

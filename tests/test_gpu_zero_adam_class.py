@@ -72,3 +72,42 @@ def test_zero_adam_object_on_the_demo_mlp():
     diff = np.abs(gu.to_host_f32(opt.master)[:numel] - w_ref)
     assert np.median(diff) < 1e-4
     assert diff.max() <= 3 * 2 * lr
+
+
+def test_pointer_array_and_a_replaced_gradient_buffer():
+    """The same step through a list of gradient buffers and through a PointerArray of them
+    gives the same bits; ZeroAdam, which keeps a PointerArray of its buffers, steps on a
+    gradient buffer that replaced one of them."""
+    import zero_partitioned_mixed_adam_gb300 as za
+    world = 4
+    opts = []
+    for replace in (False, True):
+        model = _model().cuda()
+        opt = ZeroAdam(model.parameters(), lr=1e-2, world=world)
+        for k in range(world):
+            g = opt.grads[k]
+            g.copy_(torch.randn(g.numel(), generator=torch.Generator().manual_seed(k)).to(
+                torch.bfloat16))
+        x = torch.randn(opt.grads[2].numel(), generator=torch.Generator().manual_seed(99)).to(
+            device=opt.grads[2].device, dtype=torch.bfloat16)
+        if replace:   # rank 2's gradients in a new buffer; the old one keeps other values
+            opt.grads[2] = x
+        else:
+            opt.grads[2].copy_(x)
+        opt.step(check=True)
+        opts.append(opt)
+    torch.cuda.synchronize()
+    for name in ("master", "m", "v", "flat_params"):   # bit for bit
+        assert torch.equal(getattr(opts[0], name).view(torch.int16),
+                           getattr(opts[1], name).view(torch.int16)), name
+    # the raw call: a list and a PointerArray of the same buffers
+    o = opts[0]
+    outs = []
+    for grads in (list(o.grads), za.pointer_array(o.grads)):
+        w, m, v = o.master.clone(), o.m.clone(), o.v.clone()
+        p = torch.empty_like(o.flat_params)
+        za.zero_adam_step(o.plan, za.ZERO_ALL_RANKS, grads, w, m, v, p, lr=1e-2, t=2)
+        outs.append((w, m, v, p))
+    za.check_device("pointer array step")
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))

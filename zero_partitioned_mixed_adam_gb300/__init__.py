@@ -114,6 +114,38 @@ def _addr(x) -> int:
     return int(x.data_ptr())
 
 
+class PointerArray:
+    """The device addresses of a fixed list of buffers, marshalled once.
+
+    Pass it wherever a call takes a sequence of buffers (gradients, shards): a
+    training loop hands the same buffers to every step, and building the C
+    array of N addresses is most of a call's host time at large N.  It keeps
+    references to the buffers, so they stay alive as long as the array does;
+    it records each buffer's address when built and does not follow a buffer
+    whose storage is replaced afterwards (build a new array then)."""
+
+    __slots__ = ("arr", "buffers")
+
+    def __init__(self, buffers):
+        self.buffers = tuple(buffers)
+        self.arr = (ctypes.c_void_p * len(self.buffers))(*[_addr(b) for b in self.buffers])
+
+    def __len__(self) -> int:
+        return len(self.buffers)
+
+
+def pointer_array(buffers) -> PointerArray:
+    """A reusable PointerArray of `buffers` (tensors or raw addresses)."""
+    return PointerArray(buffers)
+
+
+def _ptrs(buffers):
+    """The C array of addresses: a PointerArray's own, else built from the sequence."""
+    if isinstance(buffers, PointerArray):
+        return buffers.arr
+    return (ctypes.c_void_p * len(buffers))(*[_addr(b) for b in buffers])
+
+
 def _stream_handle(stream) -> int:
     if stream is None:
         try:
@@ -140,13 +172,14 @@ def zero_adam_step(plan: ZeroPlan, rank: int, grads, master, m, v, param, *, lr:
                    stream=None) -> None:
     """One fused ZeRO Adam step (reduce-scatter + Adam + bf16 all-gather) on the GPU.
 
-    grads: sequence of `world` bf16 device buffers (tensors or addresses);
+    grads: sequence of `world` bf16 device buffers (tensors or addresses), or a
+    PointerArray of them (pointer_array: marshalled once, reused every step);
     master/m/v: fp32 device buffers; param: bf16 device buffer.  Layouts and
     index conventions are those of zero_adam_step in include/zeroadam.h.
     """
-    ptrs = (ctypes.c_void_p * len(grads))(*[_addr(g) for g in grads])
     if len(grads) != plan.world:
         raise ValueError(f"expected {plan.world} gradient buffers, got {len(grads)}")
+    ptrs = _ptrs(grads)
     rc = _lib.zero_adam_step(ctypes.byref(plan), rank, ptrs, grad_layout, _addr(master),
                              _addr(m), _addr(v), _addr(param), param_layout, lr, beta1, beta2,
                              eps, t, _stream_handle(stream))
@@ -163,9 +196,9 @@ def zero_adam_step_range(plan: ZeroPlan, rank: int, begin: int, end: int, grads,
     With ZERO_GRAD_WINDOW (the default here) each gradient buffer holds only the
     window: element i at grads[k][i - begin].
     """
-    ptrs = (ctypes.c_void_p * len(grads))(*[_addr(g) for g in grads])
     if len(grads) != plan.world:
         raise ValueError(f"expected {plan.world} gradient buffers, got {len(grads)}")
+    ptrs = _ptrs(grads)
     rc = _lib.zero_adam_step_range(ctypes.byref(plan), rank, begin, end, ptrs, grad_layout,
                                    _addr(master), _addr(m), _addr(v), _addr(param), param_layout,
                                    lr, beta1, beta2, eps, t, _stream_handle(stream))
@@ -177,7 +210,7 @@ def zero3_unit_gather(unit_plan: ZeroPlan, shards, full, stream=None) -> None:
     """ZeRO-3 unit all-gather: the `world` bf16 shards -> the unit's full bf16 buffer."""
     if len(shards) != unit_plan.world:
         raise ValueError(f"expected {unit_plan.world} shards, got {len(shards)}")
-    ptrs = (ctypes.c_void_p * len(shards))(*[_addr(s) for s in shards])
+    ptrs = _ptrs(shards)
     rc = _lib.zero3_unit_gather(ctypes.byref(unit_plan), ptrs, _addr(full),
                                 _stream_handle(stream))
     if rc != ZERO_OK:
@@ -193,8 +226,7 @@ def zero3_unit_step(unit_plan: ZeroPlan, rank: int, shards, full, grads, master,
     by zero_adam_step; the two parts' buffers must be disjoint)."""
     if len(shards) != unit_plan.world or len(grads) != unit_plan.world:
         raise ValueError(f"expected {unit_plan.world} shards and gradient buffers")
-    sp = (ctypes.c_void_p * len(shards))(*[_addr(x) for x in shards])
-    gp = (ctypes.c_void_p * len(grads))(*[_addr(g) for g in grads])
+    sp, gp = _ptrs(shards), _ptrs(grads)
     rc = _lib.zero3_unit_step(ctypes.byref(unit_plan), rank, sp, _addr(full), gp, grad_layout,
                               _addr(master), _addr(m), _addr(v), _addr(param), param_layout, lr,
                               beta1, beta2, eps, t, _stream_handle(stream))
@@ -216,7 +248,7 @@ def zero3_unit_gather_rows(shapes, world: int, shards, full, stream=None) -> Non
     n = len(shapes)
     rows = (ctypes.c_int64 * max(n, 1))(*[int(r) for r, _ in shapes])
     cols = (ctypes.c_int64 * max(n, 1))(*[int(c) for _, c in shapes])
-    ptrs = (ctypes.c_void_p * len(shards))(*[_addr(s) for s in shards])
+    ptrs = _ptrs(shards)
     rc = _lib.zero3_unit_gather_rows(n, rows, cols, world, ptrs, _addr(full),
                                      _stream_handle(stream))
     if rc != ZERO_OK:
@@ -256,7 +288,7 @@ def raw_lib() -> ctypes.CDLL:
 
 
 __all__ = ["zero_plan", "zero_adam_step", "zero_adam_step_range", "zero3_unit_gather",
-           "zero3_unit_gather_rows", "zero3_unit_step", "rows_layout", "device_status",
+           "zero3_unit_gather_rows", "pointer_array", "PointerArray", "zero3_unit_step", "rows_layout", "device_status",
            "check_device", "test_withhold_copies",
            "ZeroPlan", "ZeroError", "strerror", "version", "raw_lib", "ZERO_ALL_RANKS",
            "ZERO_GRAD_FULL", "ZERO_GRAD_SHARD", "ZERO_GRAD_WINDOW", "ZERO_GRAD_F32",

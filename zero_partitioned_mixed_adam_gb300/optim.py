@@ -20,7 +20,7 @@ from __future__ import annotations
 
 import torch
 
-from . import ZERO_ALL_RANKS, check_device, zero_adam_step, zero_plan
+from . import ZERO_ALL_RANKS, check_device, pointer_array, zero_adam_step, zero_plan
 
 
 class ZeroAdam:
@@ -42,6 +42,7 @@ class ZeroAdam:
         self.v = torch.zeros_like(self.master)
         self.flat_params = torch.empty(self.numel, dtype=torch.bfloat16, device=dev)
         self.grads = [torch.zeros(padded, dtype=torch.bfloat16, device=dev) for _ in range(world)]
+        self._grad_ptrs = pointer_array(self.grads)
         off = 0
         with torch.no_grad():
             for p in self.params:
@@ -68,7 +69,9 @@ class ZeroAdam:
         of the step was not updated."""
         self.t += 1
         b1, b2 = self.betas
-        zero_adam_step(self.plan, ZERO_ALL_RANKS, self.grads, self.master, self.m, self.v,
+        if any(a is not b for a, b in zip(self.grads, self._grad_ptrs.buffers)):
+            self._grad_ptrs = pointer_array(self.grads)   # a gradient buffer was replaced
+        zero_adam_step(self.plan, ZERO_ALL_RANKS, self._grad_ptrs, self.master, self.m, self.v,
                        self.flat_params, lr=self.lr, beta1=b1, beta2=b2, eps=self.eps, t=self.t,
                        stream=stream)
         if check:
