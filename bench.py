@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ZeRO Adam step Gelem/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
+L2_FALLBACK_BYTES = 129 << 20   # GB300's L2, when the device does not report it
 
 
 def _peaks():
@@ -62,10 +63,10 @@ def _workload(name):
     raise SystemExit(f"unknown workload {name}")
 
 
-def _bytes_per_step(wl, plan):
+def _bytes_per_step(wl, shard):
     """Algorithmic bytes of one step: (2N + 26) per stepped element ((4N + 26) with fp32
     gradients)."""
-    n = _elements(wl, plan)
+    n = _elements(wl, shard)
     return ((4 if wl.grad_f32 else 2) * wl.world + 26) * n
 
 
@@ -73,11 +74,12 @@ def _grad_flags(za, wl):
     return (za.ZERO_GRAD_F32 if wl.grad_f32 else 0) | (za.ZERO_ACC_BF16 if wl.acc_bf16 else 0)
 
 
-def _elements(wl, plan):
+def _elements(wl, shard):
+    """Elements one step updates: all of them, or the stepped rank's real ones."""
     if wl.rank < 0:
         return wl.numel
-    lo = wl.rank * plan.shard
-    return max(0, min(plan.shard, wl.numel - lo))
+    lo = wl.rank * shard
+    return max(0, min(shard, wl.numel - lo))
 
 
 class ClockSampler:
@@ -193,7 +195,7 @@ class Replica:
         S, P = plan.shard, plan.padded
         single = wl.rank >= 0
         self.lo = wl.rank * S if single else 0
-        self.n = n = _elements(wl, plan)
+        self.n = n = _elements(wl, plan.shard)
         self.unit = wl.name.startswith("unit")
         g_len = S if wl.grad_layout == "shard" else P
         s_len = S if single else P
@@ -222,11 +224,11 @@ class Replica:
         self.kernels = []
         if self.unit and self.unit_mode == "fused":
             self.kernels.append((self.unit_step_kernel_name(),
-                                 4 * wl.numel + _bytes_per_step(wl, plan)))
+                                 4 * wl.numel + _bytes_per_step(wl, plan.shard)))
         else:
             if self.unit:
                 self.kernels.append((self.gather_kernel_name(), 4 * wl.numel))
-            self.kernels.append((self.step_kernel_name(), _bytes_per_step(wl, plan)))
+            self.kernels.append((self.step_kernel_name(), _bytes_per_step(wl, plan.shard)))
 
     def gather_kernel_name(self):
         """The library copies on the TMA engine when the shard is a multiple of 8
@@ -243,7 +245,7 @@ class Replica:
         aligned = all(x.data_ptr() % 16 == 0
                       for x in self.shards + [self.full] + self.g + [self.w, self.m, self.v,
                                                                      self.p])
-        small = 4 * self.wl.numel + _bytes_per_step(self.wl, self.plan) <= (512 << 20)
+        small = 4 * self.wl.numel + _bytes_per_step(self.wl, self.plan.shard) <= (512 << 20)
         plain = not (self.wl.grad_f32 or self.wl.acc_bf16)
         if (self.wl.numel >= 8 and self.n >= 8 and self.plan.shard % 8 == 0 and aligned and small
                 and plain):
@@ -329,7 +331,8 @@ class L2Flush:
 
     def __init__(self, dev):
         import torch
-        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
+        props = torch.cuda.get_device_properties(dev)
+        l2 = getattr(props, "L2_cache_size", 0) or L2_FALLBACK_BYTES
         self.nbytes = 2 * l2
         self.a = torch.empty(self.nbytes // 4, dtype=torch.float32, device=dev)
         self.b = torch.zeros(self.nbytes // 4, dtype=torch.float32, device=dev)
@@ -342,7 +345,8 @@ class L2Flush:
     @staticmethod
     def needed(step_bytes, dev):
         import torch
-        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
+        props = torch.cuda.get_device_properties(dev)
+        l2 = getattr(props, "L2_cache_size", 0) or L2_FALLBACK_BYTES
         return step_bytes < 4 * l2
 
 
@@ -431,6 +435,16 @@ def _cpu_oracle_sample(wl, seconds):
                                     "one host thread"}
 
 
+def _reference_flush_bytes(args, wl):
+    """The L2 flush our arm would apply to this workload on a GB300 (L2 of 129 MiB), so
+    that both arms describe the same configuration; the reference arm itself runs on
+    the host and touches no GPU."""
+    if args.l2 == "none" or (args.l2 == "auto"
+                             and _workload_bytes(wl) >= 4 * L2_FALLBACK_BYTES):
+        return None
+    return 2 * L2_FALLBACK_BYTES
+
+
 def run_reference(args, wl):
     """The reference arm: the CPU oracle timed on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -454,7 +468,8 @@ def run_reference(args, wl):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * el / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": _config(wl, None), "cpu_baseline": cb,
+        "config": _config(wl, args.unit_mode, _reference_flush_bytes(args, wl)),
+        "cpu_baseline": cb,
         "e2e": {"value": v, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -523,11 +538,20 @@ def aggregate(ms_local: float, elems_per_rank: int, world_size: int, dist=None, 
     return ms, world_size * elems_per_rank / (ms * 1e-3) / 1e9
 
 
-def _config(wl, rep, flush=None):
+def _workload_bytes(wl):
+    """Algorithmic bytes of one step of the workload: the step's (2N + 26) per stepped
+    element, plus 4 per unit element for a ZeRO-3 unit's gather."""
+    shard = -(-wl.numel // wl.world)
+    return (4 * wl.numel if wl.name.startswith("unit") else 0) + _bytes_per_step(wl, shard)
+
+
+def _config(wl, unit_mode="fused", flush_bytes=None):
+    """The workload's description, the same for both arms: sizes, layouts, distributions,
+    the algorithmic bytes per step and the L2 handling between timed steps."""
     l2 = "inputs larger than L2 (no flush)"
-    if flush is not None:
-        l2 = (f"L2 flushed before every timed step: a {flush.nbytes >> 20} MiB write, then a "
-              f"{flush.nbytes >> 20} MiB read (clean lines), outside the timed launches; "
+    if flush_bytes is not None:
+        l2 = (f"L2 flushed before every timed step: a {flush_bytes >> 20} MiB write, then a "
+              f"{flush_bytes >> 20} MiB read (clean lines), outside the timed launches; "
               "ms_per_step is the sum of the step's launch times")
     c = {"workload": wl.name, "numel": wl.numel, "world": wl.world,
          "rank": "all" if wl.rank < 0 else wl.rank, "grad_layout": wl.grad_layout,
@@ -535,16 +559,13 @@ def _config(wl, rep, flush=None):
          "l2": l2, "parallelism": "replicas",
          "state": "fp32 master/m/v, bf16 params",
          "gradients": "fp32" if wl.grad_f32 else "bf16",
-         "reduce": "bf16-rounded sum" if wl.acc_bf16 else "fp32 sum"}
-    if rep is not None:
-        c["shard"] = rep.plan.shard
-        c["bytes_per_step"] = rep.step_bytes()
-        c["launches_per_step"] = [k for k, _ in rep.kernels]
-        if rep.unit:
-            c["unit_step"] = ("zero3_unit_step: the gather of the N shards and rank 0's step on "
-                              "its shard in one call" if rep.unit_mode == "fused" else
-                              "zero3_unit_gather of the N shards, then rank 0's step on its shard")
-            c["elements"] = "unit elements U per step"
+         "reduce": "bf16-rounded sum" if wl.acc_bf16 else "fp32 sum",
+         "shard": -(-wl.numel // wl.world), "bytes_per_step": _workload_bytes(wl)}
+    if wl.name.startswith("unit"):
+        c["unit_step"] = ("zero3_unit_step: the gather of the N shards and rank 0's step on "
+                          "its shard in one call" if unit_mode == "fused" else
+                          "zero3_unit_gather of the N shards, then rank 0's step on its shard")
+        c["elements"] = "unit elements U per step"
     return c
 
 
@@ -638,7 +659,9 @@ def run_ours(args, wl):
             "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": world_size,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": _config(wl, rep, flush),
+            "data": "synthetic",
+            "config": _config(wl, rep.unit_mode, flush.nbytes if flush is not None else None),
+            "launches_per_step": [k for k, _ in rep.kernels],
             "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak,
             "roofline": {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                          "frac": dom["gbs"] / peak, "traffic": traffic,

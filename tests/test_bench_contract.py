@@ -45,6 +45,25 @@ def test_reference_arm_line():
     assert cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    c = d["config"]   # the workload's own description, as our arm prints it
+    assert c["shard"] == 250_001 and c["bytes_per_step"] == (2 * 4 + 26) * 1_000_003
+    assert c["l2"].startswith("L2 flushed before every timed step: a 258 MiB write")
+
+
+def test_config_describes_the_workload_alone():
+    """Both arms build config from the workload: its sizes, the algorithmic bytes of a
+    step ((2N + 26) per stepped element, plus 4 per unit element for a ZeRO-3 unit) and
+    the L2 handling; nothing in it depends on the implementation that ran."""
+    import bench
+    cases = {"1p3b": (81_250_000, 58 * 1_300_000_000),
+             "7b_rank3": (875_000_000, 42 * 875_000_000),
+             "unit:16777216:8": (2_097_152, 4 * 16_777_216 + 42 * 2_097_152),
+             "shard:202383360:64": (3_162_240, 154 * 3_162_240)}
+    for name, (shard, nbytes) in cases.items():
+        c = bench._config(bench._workload(name))
+        assert (c["shard"], c["bytes_per_step"]) == (shard, nbytes), name
+        assert c["l2"] == "inputs larger than L2 (no flush)"
+    assert "unit_step" in bench._config(bench._workload("unit:16777216:8"))
 
 
 def test_warmup_below_three_is_refused():
@@ -74,6 +93,9 @@ def test_our_arm_line():
     for k in ("sm_mhz", "sm_max_mhz", "reasons"):
         assert k in c, k
     assert d["config"]["l2"].startswith("L2 flushed")   # tiny moves less than 4 L2 sizes
+    assert d["launches_per_step"] == ["zero_adam_step_kernel"]
+    ref = _line("--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3")
+    assert ref["config"] == d["config"]   # both arms describe the same configuration
 
 
 def test_workload_names():
