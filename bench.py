@@ -1005,10 +1005,13 @@ def prefetch_pass(layers, gather, compute, main_stream, side_stream):
 
 def run_zero3_prefetch(args):
     """ZeRO-3 forward with prefetch: L Llama-7B-layer units, FSDP2-style row-sharded over
-    N ranks.  Layer l's compute (a stand-in: one bf16 GEMM of T tokens on the unit's
-    first 4096x4096 weight) runs on the main stream while the gather of layer l+1 runs
-    on a side stream into the other of two unit buffers (the memory peak is two
-    unfolded units).  Timed serial (gather then compute on one stream) and pipelined."""
+    N ranks.  Layer l's compute runs on the main stream while the gather of layer l+1
+    runs on a side stream into the other of two unit buffers (the memory peak is two
+    unfolded units).  The compute is a stand-in on the gathered weights: the layer's
+    seven linear maps on T tokens (--stand-in layer: q, k, v, o, gate, up, down as bf16
+    GEMMs, attention and the activation left out) or one GEMM on its first 4096x4096
+    weight (--stand-in gemm).  Timed serial (gather then compute on one stream) and
+    pipelined."""
     import torch
     import synth
     import zero_partitioned_mixed_adam_gb300 as za
@@ -1028,15 +1031,34 @@ def run_zero3_prefetch(args):
                    x.data_ptr(), 0)
     x = x.view(torch.bfloat16).view(T, 4096)
     y = torch.empty(T, 4096, dtype=torch.bfloat16, device=dev)
+    offs, o = [], 0
+    for rows, cols in LLAMA_LAYER:
+        offs.append(o)
+        o += rows * cols
+    act = {k: torch.empty(T, 4096, dtype=torch.bfloat16, device=dev) for k in "qkva"}
+    gate = torch.empty(T, 11008, dtype=torch.bfloat16, device=dev)
+    up = torch.empty_like(gate)
     main_s = torch.cuda.current_stream(dev)
     side = torch.cuda.Stream(dev)
 
     def gather(li, slot, stream):
         za.zero3_unit_gather_rows(LLAMA_LAYER, N, shards[li], full[slot], stream=stream)
 
+    def weight(slot, i):
+        rows, cols = LLAMA_LAYER[i]
+        return full[slot][offs[i]:offs[i] + rows * cols].view(torch.bfloat16).view(rows, cols)
+
     def compute(li, slot):
-        w = full[slot][:4096 * 4096].view(torch.bfloat16).view(4096, 4096)
-        torch.matmul(x, w.t(), out=y)
+        if args.stand_in == "gemm":
+            torch.matmul(x, weight(slot, 0).t(), out=y)
+            return
+        for i, k in enumerate("qkv"):
+            torch.matmul(x, weight(slot, i).t(), out=act[k])
+        torch.matmul(act["v"], weight(slot, 3).t(), out=act["a"])   # o: attention left out
+        torch.matmul(act["a"], weight(slot, 4).t(), out=gate)
+        torch.matmul(act["a"], weight(slot, 5).t(), out=up)
+        gate.mul_(up)                                               # activation left out
+        torch.matmul(gate, weight(slot, 6).t(), out=y)
 
     def serial():
         for li in range(L):
@@ -1080,7 +1102,10 @@ def run_zero3_prefetch(args):
         "data": "synthetic",
         "config": {"workload": "zero3_prefetch", "layers": L, "world": N,
                    "unit": "Llama-7B layer, 202,383,360 elements, FSDP2-style row shards",
-                   "tokens": T, "stand_in_compute": "bf16 GEMM [T,4096]x[4096,4096]^T (cuBLAS)",
+                   "tokens": T, "stand_in_compute": (
+                       "one bf16 GEMM [T,4096]x[4096,4096]^T (cuBLAS)" if args.stand_in == "gemm"
+                       else "the layer's seven linear maps on T tokens with its gathered "
+                            "weights (bf16 GEMMs, cuBLAS; attention and activation left out)"),
                    "buffers": "two unfolded units (double buffering)",
                    "elements": "unit elements gathered per pass"},
         "serial_ms": t_ser, "pipelined_ms": t_pipe, "gathers_only_ms": t_g,
@@ -1116,6 +1141,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=8, help="zero3_prefetch: units per pass")
     ap.add_argument("--prefetch-world", type=int, default=8, help="zero3_prefetch: ranks")
     ap.add_argument("--tokens", type=int, default=4096, help="zero3_prefetch: GEMM rows")
+    ap.add_argument("--stand-in", choices=("layer", "gemm"), default="layer",
+                    help="zero3_prefetch: each layer's compute, its seven linear maps on the "
+                         "tokens (layer) or one 4096x4096 GEMM (gemm)")
     ap.add_argument("--grad-variant", choices=("bf16", "f32", "bf16sum"), default="bf16",
                     help="gradients in bf16 (the method), fp32 (the page's runnable demo), or "
                          "bf16 with the sum over ranks rounded to bf16 after every addition")
