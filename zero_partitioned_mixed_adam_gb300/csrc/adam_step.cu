@@ -106,15 +106,20 @@ __device__ __forceinline__ float acc_add(float acc, float x) {
 // Adam with bias correction on one element, in ZeroAdam.step's order.
 //
 // A zero numerator skips its division: for x > 0, (+-0) / x is exactly +-0,
-// the value the IEEE division returns.  bc1 = 1 - b1^t and bc2 = 1 - b2^t are
-// > 0 (beta in [0, 1), t >= 1); the last division is skipped only when its
-// denominator is > 0 (0 / 0 still goes through the division and gives NaN).
+// the value the IEEE division returns.  That includes the average over ranks
+// when N is not a power of two (a sum of exactly zero gradients divided by N:
+// at N = 5..7 with a tenth of the sums zero, the division's slow path took the
+// staged kernel from 0.96-1.02 to 0.79-0.85 of the copy peak on GB300).
+// bc1 = 1 - b1^t and bc2 = 1 - b2^t are > 0 (beta in [0, 1), t >= 1); the
+// last division is skipped only when its denominator is > 0 (0 / 0 still goes
+// through the division and gives NaN).
 // Elements whose gradient is exactly zero every step (untouched rows, dead
 // units; the GPT-2 workload's 10 % mask) keep m = v = 0, and without the
 // shortcut their divisions take the slow path of the IEEE division sequence.
 __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, float& w, float& m,
                                              float& v) {
-  const float g = s.pow2_world ? __fmul_rn(gsum, s.inv_world) : __fdiv_rn(gsum, s.world);
+  const float g = s.pow2_world ? __fmul_rn(gsum, s.inv_world)
+                               : (gsum == 0.0f ? gsum : __fdiv_rn(gsum, s.world));
   m = __fadd_rn(__fmul_rn(m, s.b1), __fmul_rn(s.omb1, g));
   v = __fadd_rn(__fmul_rn(v, s.b2), __fmul_rn(__fmul_rn(s.omb2, g), g));
   const float m_hat = (m == 0.0f) ? m : __fdiv_rn(m, s.bc1);
@@ -135,7 +140,14 @@ __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, f
 // depending on the data, this form 1.03-1.05 at 22 warps).
 __device__ __forceinline__ void adam_element_uniform(float gsum, const AdamScalars& s, float& w,
                                                      float& m, float& v) {
-  const float g = s.pow2_world ? __fmul_rn(gsum, s.inv_world) : __fdiv_rn(gsum, s.world);
+  float g;
+  if (s.pow2_world) {  // the same for every thread of the launch
+    g = __fmul_rn(gsum, s.inv_world);
+  } else {
+    const bool gz = gsum == 0.0f;
+    const float gq = __fdiv_rn(gz ? 1.0f : gsum, s.world);
+    g = gz ? gsum : gq;
+  }
   m = __fadd_rn(__fmul_rn(m, s.b1), __fmul_rn(s.omb1, g));
   v = __fadd_rn(__fmul_rn(v, s.b2), __fmul_rn(__fmul_rn(s.omb2, g), g));
   const bool mz = m == 0.0f, vz = v == 0.0f;
@@ -197,9 +209,11 @@ __device__ __forceinline__ void sum_grads8(const StepArgs<CAP>& a, int world, in
   for (int j = 0; j < 8; ++j) acc[j] = -0.0f;
   if (a.gvec) {
     // Ranks in groups: all of a group's 16-byte loads are issued before any
-    // of them is consumed.
+    // of them is consumed.  The any-N instance (NT = 0) takes groups of 4
+    // (2 for fp32 gradients), so that it fits two blocks per SM without
+    // spilling (see zero_adam_step_kernel).
     constexpr int GMAX = GF32 ? 8 : 16;
-    constexpr int G = (NT > 0 && NT <= GMAX) ? NT : 8;
+    constexpr int G = (NT > 0 && NT <= GMAX) ? NT : NT > 0 ? 8 : GF32 ? 2 : 4;
 #pragma unroll 1
     for (int k0 = 0; k0 < world; k0 += G) {
       GradVec<GF32> r[G];
@@ -272,8 +286,13 @@ __device__ __forceinline__ void step_element(const StepArgs<CAP>& a, int world, 
   a.param[e] = f32_to_bf16_rn(w);
 }
 
+// The any-N instance (NT = 0: N read at run time, the rank loop not unrolled)
+// is held to two blocks per SM, as the fixed-N instances reach on their own
+// (about 60 registers): at one block per SM (86 registers, groups of 8) it
+// streamed 0.64-0.87 of the copy peak at N = 3, 5, 6, 7, 12, 48 on GB300, and
+// 0.94-1.00 with groups of 4 and two blocks per SM (64 registers, no spills).
 template <int NT, int CAP, bool GF32, bool ABF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, NT == 0 ? 2 : 1)
     zero_adam_step_kernel(const __grid_constant__ StepArgs<CAP> a) {
   const int world = NT > 0 ? NT : a.world;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
