@@ -342,14 +342,17 @@ __device__ int g_step_status;
 //
 // Two shapes, chosen by N (measured on GB300 against the register-staged
 // kernel, bit-exact in every case): G = 8, EPT = 4, 22 consumer warps, 3
-// stages of 44 KB for 5 <= N < 40 (N = 5: 0.68 -> 0.93 of the copy peak,
-// N = 12: 0.72 -> 1.02, N = 32: 0.93 -> 1.03 on a 16.8M-element shard; at N = 8
+// stages of 44 KB for 5 <= N < 40 (against the register-staged kernel's
+// any-N instance, 2e8 elements: N = 5 0.958 vs 0.956 of the copy peak, with a
+// tenth of the gradients exactly zero 0.906 vs 0.878; N = 12 1.065 vs 1.023;
+// N = 32: 0.93 -> 1.03 on a 16.8M-element shard; at N = 8
 // 1.03-1.05 with and without exact-zero gradients; at N = 16 1.058 on the 1.3B
 // workload, level with an earlier kernel that also staged master/m/v through
 // the ring behind 8 consumer warps, which fell to 0.86 when 10 % of the
 // gradients were exact zeros while this one held 1.06); G = 32, EPT = 2, 16
-// consumer warps, 3 stages of 64 KB for N >= 40 (N = 64: 0.92 -> 0.975 on a
-// 3.16M-element shard, 0.99 -> 1.00 on 8.4M).
+// consumer warps, 3 stages of 64 KB for N >= 40 (N = 48: 1.022 vs 0.943 for the
+// any-N instance; N = 64: 0.92 -> 0.975 on a 3.16M-element shard, 0.99 -> 1.00
+// on 8.4M).
 
 template <int CAP>
 struct GradStagedArgs {
