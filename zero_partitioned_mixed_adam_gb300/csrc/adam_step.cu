@@ -41,6 +41,9 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kTableRuntime = 1024;  // gradient-pointer table of the any-N kernel
+// 1 when the register-staged kernel's instance has a fixed power-of-two N.
+template <int NT>
+constexpr int kPow2 = (NT > 0 && (NT & (NT - 1)) == 0) ? 1 : 0;
 
 // Loads.  The gradients are never written while the kernel runs, so they may
 // take the read-only (non-coherent) path.  master/m/v are read and then
@@ -116,10 +119,18 @@ __device__ __forceinline__ float acc_add(float acc, float x) {
 // Elements whose gradient is exactly zero every step (untouched rows, dead
 // units; the GPT-2 workload's 10 % mask) keep m = v = 0, and without the
 // shortcut their divisions take the slow path of the IEEE division sequence.
+// POW2 = 1: N is a power of two, known when the kernel is compiled (the
+// register-staged kernel's fixed-N instances), so the average is always the
+// exact multiplication by 1/N and no division code is generated; POW2 = 0:
+// decided at run time from s.pow2_world.
+template <int POW2>
 __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, float& w, float& m,
                                              float& v) {
-  const float g = s.pow2_world ? __fmul_rn(gsum, s.inv_world)
-                               : (gsum == 0.0f ? gsum : __fdiv_rn(gsum, s.world));
+  float g;
+  if (POW2 || s.pow2_world)
+    g = __fmul_rn(gsum, s.inv_world);
+  else
+    g = gsum == 0.0f ? gsum : __fdiv_rn(gsum, s.world);
   m = __fadd_rn(__fmul_rn(m, s.b1), __fmul_rn(s.omb1, g));
   v = __fadd_rn(__fmul_rn(v, s.b2), __fmul_rn(__fmul_rn(s.omb2, g), g));
   const float m_hat = (m == 0.0f) ? m : __fdiv_rn(m, s.bc1);
@@ -130,11 +141,15 @@ __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, f
 }
 
 // The same update with the zero-numerator shortcut taken without a branch:
-// every lane runs the three divisions on normal operands (1.0 stands in for a
-// zero numerator, and 1/1 for the last division's shortcut case), then
-// selects the shortcut's result.  The values are those of adam_element bit
-// for bit.  The staged kernels use this form: with some exact-zero gradients
-// (the GPT-2 workload's 10 % mask) the branching form diverges within warps,
+// every lane runs the divisions and the square root on normal operands (1.0
+// stands in for a zero numerator, and 1/1 for the last division's shortcut
+// case; the square root of v_hat = +-0 is +-0, taken from v_hat), then selects
+// the shortcut's result.  With a tenth of the gradients exactly zero the
+// square root of 0 had cost 1 % at N = 8 and 6 % at N = 5 on GB300; in the
+// register-staged kernel's branching form the same guard was slower.  The
+// values are those of adam_element bit for bit.  The staged kernels use this
+// form: with some exact-zero gradients (the GPT-2 workload's 10 % mask) the
+// branching form diverges within warps,
 // and the staged kernels' best consumer count then moved with the fraction of
 // zeros (measured on GB300 at N = 8: 24 warps 1.00-1.05 of the copy peak
 // depending on the data, this form 1.03-1.05 at 22 warps).
@@ -155,7 +170,8 @@ __device__ __forceinline__ void adam_element_uniform(float gsum, const AdamScala
   const float vq = __fdiv_rn(vz ? 1.0f : v, s.bc2);
   const float m_hat = mz ? m : mq;
   const float v_hat = vz ? v : vq;
-  const float denom = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
+  const float rt = __fsqrt_rn(vq);  // a normal operand: 1 / bc2 when v == 0
+  const float denom = __fadd_rn(vz ? v_hat : rt, s.eps);  // sqrt(+-0) = +-0
   const float num = __fmul_rn(s.lr, m_hat);
   const bool z = num == 0.0f && denom > 0.0f;
   const float q = __fdiv_rn(z ? 1.0f : num, z ? 1.0f : denom);
@@ -279,7 +295,7 @@ __device__ __forceinline__ void step_element(const StepArgs<CAP>& a, int world, 
 #pragma unroll 1
   for (int k = 0; k < world; ++k) acc = acc_add<ABF16>(acc, grad_scalar<GF32>(a.g[k], e));
   float w = ld_state(a.master + e), mm = ld_state(a.m + e), vv = ld_state(a.v + e);
-  adam_element(acc, a.s, w, mm, vv);
+  adam_element<kPow2<NT>>(acc, a.s, w, mm, vv);
   a.master[e] = w;
   a.m[e] = mm;
   a.v[e] = vv;
@@ -287,12 +303,14 @@ __device__ __forceinline__ void step_element(const StepArgs<CAP>& a, int world, 
 }
 
 // The any-N instance (NT = 0: N read at run time, the rank loop not unrolled)
-// is held to two blocks per SM, as the fixed-N instances reach on their own
-// (about 60 registers): at one block per SM (86 registers, groups of 8) it
-// streamed 0.64-0.87 of the copy peak at N = 3, 5, 6, 7, 12, 48 on GB300, and
-// 0.94-1.00 with groups of 4 and two blocks per SM (64 registers, no spills).
+// is held to two blocks per SM (at most 64 registers): with groups of 8 it used
+// 86 registers, fit one block per SM and streamed 0.64-0.87 of the copy peak at
+// N = 3, 5, 6, 7, 12, 48 on GB300, against 0.94-1.00 with groups of 4 at two
+// blocks.  The fixed-N instances get no minimum (0 leaves the compiler's own
+// choice, 56-61 registers: two blocks per SM); a minimum of one block let the
+// compiler take 76-94 registers in several of them and cost up to 3 %.
 template <int NT, int CAP, bool GF32, bool ABF16>
-__global__ void __launch_bounds__(kThreads, NT == 0 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, NT == 0 ? 2 : 0)
     zero_adam_step_kernel(const __grid_constant__ StepArgs<CAP> a) {
   const int world = NT > 0 ? NT : a.world;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, NT == 0 ? 2 : 1)
     load_f32x8(a.m + e0, a.svec, mm);
     load_f32x8(a.v + e0, a.svec, vv);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) adam_element(acc[j], a.s, w[j], mm[j], vv[j]);
+    for (int j = 0; j < 8; ++j) adam_element<kPow2<NT>>(acc[j], a.s, w[j], mm[j], vv[j]);
     store_f32x8(a.master + e0, a.svec, w);
     store_f32x8(a.m + e0, a.svec, mm);
     store_f32x8(a.v + e0, a.svec, vv);
@@ -547,7 +565,7 @@ __device__ void staged_tail(const GradStagedArgs<CAP>& a, int t) {
   float acc = -0.0f;
   for (int r = 0; r < a.world; ++r) acc = __fadd_rn(acc, bf16_to_f32(ld_grad(a.g[r] + e)));
   float w = ld_state(a.master + e), mm = ld_state(a.m + e), vv = ld_state(a.v + e);
-  adam_element(acc, a.s, w, mm, vv);
+  adam_element<0>(acc, a.s, w, mm, vv);
   a.master[e] = w;
   a.m[e] = mm;
   a.v[e] = vv;
@@ -685,7 +703,7 @@ __device__ void grad_reg_consumer(const GradStagedArgs<CAP>& a, int t) {
     for (int k = 0; k < 4; ++k)
       if (k < a.world) accumulate_bf16x8(acc, r[k]);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) adam_element(acc[j], a.s, w[j], mm[j], vv[j]);
+    for (int j = 0; j < 8; ++j) adam_element<0>(acc[j], a.s, w[j], mm[j], vv[j]);
     store_state_vec<8>(a.master + e0, w);
     store_state_vec<8>(a.m + e0, mm);
     store_state_vec<8>(a.v + e0, vv);
