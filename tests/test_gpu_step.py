@@ -420,12 +420,15 @@ def test_7b_rank3_full_size_sampled_and_prewarmed():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("world", [3, 4, 6, 8, 12])
 @pytest.mark.parametrize("eps", [1e-8, 0.0])
-def test_zero_gradients_and_signed_zeros(eps):
+def test_zero_gradients_and_signed_zeros(eps, world):
     """Exact +-0 gradients that persist over steps (m = v = 0 stays), +-0 master weights,
-    and eps = 0 (where 0/0 must still give NaN): the kernel's zero-numerator shortcut
-    must agree with the oracle bit for bit."""
-    numel, world = 50_003, 4
+    and eps = 0 (where 0/0 must still give NaN): the kernels' zero shortcuts (Adam's
+    divisions, the average's division when N is not a power of two, the square root of
+    v = 0) must agree with the oracle bit for bit.  N = 3: the register-staged kernel's
+    any-N instance; 4: a fixed instance; 6, 8, 12: the gradient-staged kernel."""
+    numel = 50_003
     pr = Problem(numel, world, eps=eps)
     rng = np.random.default_rng(31)
     zero_rows = rng.random(numel) < 0.3
