@@ -167,6 +167,13 @@ def kernel_source_hash(kernel_src):
     return code_hash(kernel_src, *headers)
 
 
+def traffic_key(kernel, wl):
+    """Key of a kernel's traffic record: kernel/N, and the gradient variant when it is not
+    the method's bf16 gradients with an fp32 sum (other bytes per element)."""
+    variant = "/f32" if wl.grad_f32 else "/bf16sum" if wl.acc_bf16 else ""
+    return f"{kernel}/N{wl.world}{variant}"
+
+
 def _traffic_record(kernel_src):
     """DRAM traffic per element from the committed ncu summary, if it was taken on
     the current code of the kernel's source file and headers (else None)."""
@@ -641,7 +648,7 @@ def run_ours(args, wl):
         src, units = "unit_gather.cu", wl.numel       # per unit element
     if src:
         rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc", src))
-        rec = (rec or {}).get(f"{dom['kernel']}/N{wl.world}")
+        rec = (rec or {}).get(traffic_key(dom["kernel"], wl))
         if rec:
             traffic = rec["dram_bytes_per_element"] * units
 

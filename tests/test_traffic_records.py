@@ -43,9 +43,10 @@ def test_records_are_consistent():
             continue
         assert len(key) == 64
         for name, r in kernels.items():
-            kernel, world = name.split("/N")
+            kernel, rest = name.split("/N")
+            world, _, variant = rest.partition("/")
             assert kernel.startswith(("zero_adam_step", "zero3_unit_gather", "zero3_unit_step"))
-            assert int(world) >= 1
+            assert int(world) >= 1 and variant in ("", "f32", "bf16sum")
             per = (r["dram_read_bytes"] + r["dram_write_bytes"]) / r["elements"]
             assert abs(per - r["dram_bytes_per_element"]) < 1e-4
             # every input byte is read once: the reads match the algorithmic reads
@@ -59,3 +60,14 @@ def test_records_are_consistent():
             assert lower * alg < per <= 1.02 * alg, name
             n += 1
     assert n >= 4
+
+
+def test_traffic_key_names_the_gradient_variant():
+    from synth import configs as C
+    import dataclasses
+    wl = C.WORKLOADS["gpt2"]
+    assert bench.traffic_key("zero_adam_step_kernel", wl) == "zero_adam_step_kernel/N8"
+    f32 = dataclasses.replace(wl, grad_f32=True)
+    s16 = dataclasses.replace(wl, acc_bf16=True)
+    assert bench.traffic_key("zero_adam_step_kernel", f32) == "zero_adam_step_kernel/N8/f32"
+    assert bench.traffic_key("zero_adam_step_kernel", s16) == "zero_adam_step_kernel/N8/bf16sum"
