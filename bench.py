@@ -600,7 +600,6 @@ def run_ours(args, wl):
         rep.step(t, stream)
     rep.fill_grads(wl.prewarm + 1)
 
-    nk = len(rep.kernels)
     need = L2Flush.needed(rep.step_bytes(), dev) if args.l2 == "auto" else args.l2 == "flush"
     flush = L2Flush(dev) if need else None
     # The clock sampler starts before the warm-up steps, which run as the timed steps do
@@ -634,7 +633,7 @@ def run_ours(args, wl):
                            "gbs": nbytes / (statistics.mean(ms) * 1e-3) / 1e9})
     elems = rep.unit_elements()
     ms_step, value = aggregate(total_ms / args.steps, elems, world_size, dist, dev)
-    dom = max(per_kernel, key=lambda k: k["avg_launch_ms"] * 1)
+    dom = max(per_kernel, key=lambda k: k["avg_launch_ms"])
     peak, peak_src = _peaks()
     traffic = None
     src, units = None, 0
