@@ -174,6 +174,28 @@ def traffic_key(kernel, wl):
     return f"{kernel}/N{wl.world}{variant}"
 
 
+def launch_traffic(kernel, wl, n):
+    """DRAM bytes of one call of `kernel` (a launch, or "a+b" for a call that launches two)
+    from the committed records, or None when a record is missing or void: per unit element
+    for the gathers and the one-launch unit step, per stepped element (n) for the steps."""
+    total = 0.0
+    for k in kernel.split("+"):
+        if k == "zero3_unit_step_kernel":
+            src, units = "adam_step.cu", wl.numel
+        elif k.startswith("zero_adam_step"):
+            src, units = "adam_step.cu", n
+        elif k.startswith("zero3_unit_gather"):
+            src, units = "unit_gather.cu", wl.numel
+        else:
+            return None
+        rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc", src))
+        rec = (rec or {}).get(traffic_key(k, wl))
+        if not rec:
+            return None
+        total += rec["dram_bytes_per_element"] * units
+    return total
+
+
 def _traffic_record(kernel_src):
     """DRAM traffic per element from the committed ncu summary, if it was taken on
     the current code of the kernel's source file and headers (else None)."""
@@ -635,21 +657,7 @@ def run_ours(args, wl):
     ms_step, value = aggregate(total_ms / args.steps, elems, world_size, dist, dev)
     dom = max(per_kernel, key=lambda k: k["avg_launch_ms"])
     peak, peak_src = _peaks()
-    traffic = None
-    src, units = None, 0
-    if dom["kernel"] == "zero3_unit_step_kernel":
-        src, units = "adam_step.cu", wl.numel         # per unit element
-    elif "+" in dom["kernel"]:
-        src = None                                    # two launches: no single capture
-    elif dom["kernel"].startswith("zero_adam_step"):
-        src, units = "adam_step.cu", rep.n            # per stepped element
-    elif dom["kernel"].startswith("zero3_unit_gather"):
-        src, units = "unit_gather.cu", wl.numel       # per unit element
-    if src:
-        rec = _traffic_record(os.path.join(ROOT, "zero_partitioned_mixed_adam_gb300", "csrc", src))
-        rec = (rec or {}).get(traffic_key(dom["kernel"], wl))
-        if rec:
-            traffic = rec["dram_bytes_per_element"] * units
+    traffic = launch_traffic(dom["kernel"], wl, rep.n)
 
     e2e = None
     cpu = None

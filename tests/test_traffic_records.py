@@ -71,3 +71,15 @@ def test_traffic_key_names_the_gradient_variant():
     s16 = dataclasses.replace(wl, acc_bf16=True)
     assert bench.traffic_key("zero_adam_step_kernel", f32) == "zero_adam_step_kernel/N8/f32"
     assert bench.traffic_key("zero_adam_step_kernel", s16) == "zero_adam_step_kernel/N8/bf16sum"
+
+
+def test_two_launch_traffic_is_the_sum_of_its_records():
+    """A call that launches two kernels (a large unit's gather, then its step) reports the
+    sum of the two records; a kernel without a record gives None, not a partial sum."""
+    wl = bench._workload("unit:202383360:64")
+    S = -(-wl.numel // wl.world)
+    g = bench.launch_traffic("zero3_unit_gather_tma_kernel", wl, S)
+    st = bench.launch_traffic("zero_adam_step_tma_grad_kernel", wl, S)
+    both = bench.launch_traffic("zero3_unit_gather_tma_kernel+zero_adam_step_tma_grad_kernel", wl, S)
+    assert g and st and abs(both - (g + st)) < 1.0
+    assert bench.launch_traffic("zero3_unit_gather_tma_kernel+no_such_kernel", wl, S) is None
