@@ -25,8 +25,9 @@ import zero_partitioned_mixed_adam_gb300 as za  # noqa: E402
 LR, B1, B2, EPS = 1e-3, 0.9, 0.999, 1e-8
 
 
-def _gspec(k, t, seed=0):
-    return synth.Spec(seed=seed, stream=C.STREAM_GRAD, rank=k, step=t, sigma=1e-3)
+def _gspec(k, t, seed=0, zero_frac=0.0):
+    return synth.Spec(seed=seed, stream=C.STREAM_GRAD, rank=k, step=t, sigma=1e-3,
+                      zero_frac=zero_frac)
 
 
 def _mspec(seed=0):
@@ -169,7 +170,11 @@ def test_bucketed_schedule_on_a_side_stream(step_streams):
 
 @pytest.mark.parametrize("world", [1, 3, 4, 8, 16, 64, 65])
 @pytest.mark.parametrize("grad_f32,acc_bf16", [(True, False), (False, True), (True, True)])
-def test_gradient_variants_vs_oracle(world, grad_f32, acc_bf16):
+@pytest.mark.parametrize("zero_frac", [0.0, 0.1])
+def test_gradient_variants_vs_oracle(world, grad_f32, acc_bf16, zero_frac):
+    """The f4 variants against the oracle's, with and without a tenth of the gradient sums
+    exactly zero (a mask shared by the ranks: the zero shortcuts of Adam's divisions and,
+    at N = 3 and 65, of the average's division)."""
     numel = 70_001
     plan = za.zero_plan(numel, world)
     kind = synth.OUT_F32 if grad_f32 else synth.OUT_BF16
@@ -183,14 +188,14 @@ def test_gradient_variants_vs_oracle(world, grad_f32, acc_bf16):
     for t in (1, 2):
         hg = []
         for k in range(world):
-            gu.dev_fill_into(g[k][:numel], _gspec(k, t), 0, kind)
-            h = synth.fill_host(_gspec(k, t), 0, numel, kind)
+            gu.dev_fill_into(g[k][:numel], _gspec(k, t, zero_frac=zero_frac), 0, kind)
+            h = synth.fill_host(_gspec(k, t, zero_frac=zero_frac), 0, numel, kind)
             hg.append(np.pad(h, (0, plan.padded - numel)))
         za.zero_adam_step(plan, -1, g, w, m, v, p, lr=LR, t=t, grad_layout=flags)
         oracle.zero_step(numel, world, -1, hg, hw, hm, hv, hp, LR, B1, B2, EPS, t,
                          grad_f32=grad_f32, acc_bf16=acc_bf16)
     torch.cuda.synchronize()
-    what = f"N={world} f32={grad_f32} bf16acc={acc_bf16}"
+    what = f"N={world} f32={grad_f32} bf16acc={acc_bf16} zeros={zero_frac}"
     gu.assert_f32_close(gu.to_host_f32(w)[:numel], hw[:numel], what + " master")
     gu.assert_f32_close(gu.to_host_f32(m)[:numel], hm[:numel], what + " m")
     gu.assert_f32_close(gu.to_host_f32(v)[:numel], hv[:numel], what + " v")
