@@ -34,16 +34,20 @@ def _step_cases(n=48, seed=20261202):
         pl = FULL if rank < 0 or rng.random() < 0.6 else SHARD
         # half the cases fully aligned (the staged kernels at N >= 5), half not
         offs = (0, 0, 0) if rng.random() < 0.5 else tuple(int(x) for x in rng.integers(0, 8, 3))
-        cases.append((numel, world, rank, gl, pl, offs, i))
+        # a third of the cases without zeros, a third with 10 %, a third with 50 % of the
+        # gradient sums exactly zero (from the index: the draws above stay as they were)
+        cases.append((numel, world, rank, gl, pl, offs, i, (0.0, 0.1, 0.5)[i % 3]))
     return cases
 
 
-@pytest.mark.parametrize("numel,world,rank,gl,pl,offs,seed", _step_cases())
-def test_step_sweep(numel, world, rank, gl, pl, offs, seed):
-    pr = Problem(numel, world, rank=rank, grad_layout=gl, param_layout=pl, offs=offs, seed=seed)
+@pytest.mark.parametrize("numel,world,rank,gl,pl,offs,seed,zero_frac", _step_cases())
+def test_step_sweep(numel, world, rank, gl, pl, offs, seed, zero_frac):
+    pr = Problem(numel, world, rank=rank, grad_layout=gl, param_layout=pl, offs=offs, seed=seed,
+                 zero_frac=zero_frac)
     for t in (1, 2):
         pr.step(t)
-        pr.check(f"numel={numel} N={world} rank={rank} gl={gl} pl={pl} offs={offs} t={t}")
+        pr.check(f"numel={numel} N={world} rank={rank} gl={gl} pl={pl} offs={offs} "
+                 f"zeros={zero_frac} t={t}")
     assert za.device_status() == za.ZERO_OK
 
 
