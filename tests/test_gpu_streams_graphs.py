@@ -92,3 +92,50 @@ def test_bucket_sequence_captured_in_a_cuda_graph(world):
     assert _same(check, eager2)
     assert torch.equal(full, torch.cat(shards)[:1_000_003])
     assert za.device_status() == 0
+
+
+@pytest.mark.parametrize("world", [4, 8, 64])
+def test_unit_step_captured_in_a_cuda_graph(world):
+    """A small ZeRO-3 unit's gather + step (one launch at these sizes) captured once, with
+    the buffers passed as pointer arrays, and replayed twice: the same bits as the same
+    calls made eagerly (a loop over small units replays a graph instead of paying the host
+    marshalling and the launch for every unit)."""
+    U = 1 << 20
+    plan = za.zero_plan(U, world)
+    S = plan.shard
+    shards = [torch.full((S,), 100 + k, dtype=torch.int16, device="cuda") for k in range(world)]
+    gen = torch.Generator(device="cuda").manual_seed(world)
+    grads = [(torch.randn(S, generator=gen, device="cuda") * 1e-3).to(torch.bfloat16)
+             .view(torch.int16) for _ in range(world)]
+    w0 = torch.randn(S, generator=gen, device="cuda") * 0.02
+    sp, gp = za.pointer_array(shards), za.pointer_array(grads)
+
+    def fresh():
+        return [torch.zeros(U, dtype=torch.int16, device="cuda"), w0.clone(),
+                torch.zeros_like(w0), torch.zeros_like(w0),
+                torch.zeros(S, dtype=torch.int16, device="cuda")]
+
+    def run(bufs, t, s_arg, g_arg, stream=None):
+        full, w, m, v, p = bufs
+        za.zero3_unit_step(plan, 1, s_arg, full, g_arg, w, m, v, p, lr=1e-3, t=t,
+                           grad_layout=za.ZERO_GRAD_SHARD, param_layout=za.ZERO_PARAM_SHARD,
+                           stream=stream)
+
+    graphed = fresh()
+    run(graphed, 1, sp, gp)               # per-device set-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run(graphed, 2, sp, gp)       # t = 2 is baked into the captured launch
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    eager = fresh()
+    for t in (1, 2, 2):
+        run(eager, t, list(shards), list(grads))
+    torch.cuda.synchronize()
+    assert _same(graphed, eager)
+    assert torch.equal(graphed[0], torch.cat(shards)[:U])
+    assert za.device_status() == 0
