@@ -284,7 +284,8 @@ class Replica:
     def step_kernel_name(self):
         """The library runs the TMA-staged kernel (gradients staged in rank groups)
         for N >= 5 when every buffer is 16-byte aligned at the range's first
-        element (whole cudaMalloc buffers); the register-staged kernel otherwise."""
+        element (whole cudaMalloc buffers); the register-staged kernel otherwise
+        (its fixed-N instance, or its any-N kernel)."""
         def aligned(t, first, esize):
             return (t.data_ptr() + first * esize) % 16 == 0
         gsize = 4 if self.wl.grad_f32 else 2
@@ -292,7 +293,11 @@ class Replica:
                and all(aligned(g, self.g_first, gsize) for g in self.g)
                and all(aligned(x, 0, 4) for x in (self.w, self.m, self.v))
                and aligned(self.p, self.p_first, 2))
-        return "zero_adam_step_tma_grad_kernel" if tma else "zero_adam_step_kernel"
+        if tma:
+            return "zero_adam_step_tma_grad_kernel"
+        # the register-staged kernel: an instance per N in 1, 2, 4, ..., 64, else any-N
+        return ("zero_adam_step_kernel" if self.wl.world in (1, 2, 4, 8, 16, 32, 64)
+                else "zero_adam_step_any_kernel")
 
     def fill_grads(self, t):
         import torch

@@ -227,7 +227,7 @@ __device__ __forceinline__ void sum_grads8(const StepArgs<CAP>& a, int world, in
     // Ranks in groups: all of a group's 16-byte loads are issued before any
     // of them is consumed.  The any-N instance (NT = 0) takes groups of 4
     // (2 for fp32 gradients), so that it fits two blocks per SM without
-    // spilling (see zero_adam_step_kernel).
+    // spilling (see zero_adam_step_any_kernel).
     constexpr int GMAX = GF32 ? 8 : 16;
     constexpr int G = (NT > 0 && NT <= GMAX) ? NT : NT > 0 ? 8 : GF32 ? 2 : 4;
 #pragma unroll 1
@@ -302,16 +302,10 @@ __device__ __forceinline__ void step_element(const StepArgs<CAP>& a, int world, 
   a.param[e] = f32_to_bf16_rn(w);
 }
 
-// The any-N instance (NT = 0: N read at run time, the rank loop not unrolled)
-// is held to two blocks per SM (at most 64 registers): with groups of 8 it used
-// 86 registers, fit one block per SM and streamed 0.64-0.87 of the copy peak at
-// N = 3, 5, 6, 7, 12, 48 on GB300, against 0.94-1.00 with groups of 4 at two
-// blocks.  The fixed-N instances get no minimum (0 leaves the compiler's own
-// choice, 56-61 registers: two blocks per SM); a minimum of one block let the
-// compiler take 76-94 registers in several of them and cost up to 3 %.
+// The step over the range: 8 consecutive elements per thread and iteration
+// (grid-stride), the unaligned head and the tail one element per thread.
 template <int NT, int CAP, bool GF32, bool ABF16>
-__global__ void __launch_bounds__(kThreads, NT == 0 ? 2 : 0)
-    zero_adam_step_kernel(const __grid_constant__ StepArgs<CAP> a) {
+__device__ __forceinline__ void step_range(const StepArgs<CAP>& a) {
   const int world = NT > 0 ? NT : a.world;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -333,6 +327,27 @@ __global__ void __launch_bounds__(kThreads, NT == 0 ? 2 : 0)
   for (int64_t e = tid; e < a.head; e += nthreads) step_element<NT, CAP, GF32, ABF16>(a, world, e);
   for (int64_t e = a.head + 8 * a.nvec + tid; e < a.n; e += nthreads)
     step_element<NT, CAP, GF32, ABF16>(a, world, e);
+}
+
+// The fixed-N instances (N = 1, 2, 4, ..., 64): the compiler's own register
+// choice, 56-61 registers, fits two blocks of 512 threads per SM.  (A bound
+// of one block per SM let it take 76-94 registers in several of them, which
+// then fit one block per SM and ran up to 3 % slower.)
+template <int NT, int CAP, bool GF32, bool ABF16>
+__global__ void __launch_bounds__(kThreads)
+    zero_adam_step_kernel(const __grid_constant__ StepArgs<CAP> a) {
+  step_range<NT, CAP, GF32, ABF16>(a);
+}
+
+// The any-N instance (N read at run time, the rank loop not unrolled), held
+// to two blocks per SM (at most 64 registers): with rank groups of 8 it used
+// 86 registers, fit one block per SM and streamed 0.64-0.87 of the copy peak
+// at N = 3, 5, 6, 7, 12, 48 on GB300, against 0.94-1.00 with groups of 4 at
+// two blocks per SM.
+template <int CAP, bool GF32, bool ABF16>
+__global__ void __launch_bounds__(kThreads, 2)
+    zero_adam_step_any_kernel(const __grid_constant__ StepArgs<CAP> a) {
+  step_range<0, CAP, GF32, ABF16>(a);
 }
 
 // Status word of the staged kernels' bounded waits (read and cleared by
@@ -886,15 +901,23 @@ cudaError_t launch_world(const StepLaunch& L) {
     if (launch_tma_grad(L, a.head, a.nvec, a.gvec && a.svec && a.pvec, &err)) return err;
   }
 
-  const void* kern = reinterpret_cast<const void*>(&zero_adam_step_kernel<NT, CAP, GF32, ABF16>);
+  const void* kern;
+  if constexpr (NT == 0)
+    kern = reinterpret_cast<const void*>(&zero_adam_step_any_kernel<CAP, GF32, ABF16>);
+  else
+    kern = reinterpret_cast<const void*>(&zero_adam_step_kernel<NT, CAP, GF32, ABF16>);
   int sms = 0;
   if (device_sm_count(&sms) != 0) return cudaErrorNoDevice;
   const int64_t cap = static_cast<int64_t>(sms) * blocks_per_sm(kern);
   int64_t blocks = (a.nvec + kThreads - 1) / kThreads;
   if (blocks < 1) blocks = 1;
   if (blocks > cap) blocks = cap;
-  zero_adam_step_kernel<NT, CAP, GF32, ABF16>
-      <<<static_cast<unsigned>(blocks), kThreads, 0, L.stream>>>(a);
+  if constexpr (NT == 0)
+    zero_adam_step_any_kernel<CAP, GF32, ABF16>
+        <<<static_cast<unsigned>(blocks), kThreads, 0, L.stream>>>(a);
+  else
+    zero_adam_step_kernel<NT, CAP, GF32, ABF16>
+        <<<static_cast<unsigned>(blocks), kThreads, 0, L.stream>>>(a);
   return cudaGetLastError();
 }
 
