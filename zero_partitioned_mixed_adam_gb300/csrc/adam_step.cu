@@ -149,10 +149,10 @@ __device__ __forceinline__ void adam_element(float gsum, const AdamScalars& s, f
 // register-staged kernel's branching form the same guard was slower.  The
 // values are those of adam_element bit for bit.  The staged kernels use this
 // form: with some exact-zero gradients (the GPT-2 workload's 10 % mask) the
-// branching form diverges within warps,
-// and the staged kernels' best consumer count then moved with the fraction of
-// zeros (measured on GB300 at N = 8: 24 warps 1.00-1.05 of the copy peak
-// depending on the data, this form 1.03-1.05 at 22 warps).
+// branching form diverges within warps, and the staged kernels' best consumer
+// count then moved with the fraction of zeros (measured on GB300 at N = 8: 24
+// warps 1.00-1.05 of the copy peak depending on the data, this form 1.03-1.05
+// at 22 warps).
 __device__ __forceinline__ void adam_element_uniform(float gsum, const AdamScalars& s, float& w,
                                                      float& m, float& v) {
   float g;
